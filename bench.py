@@ -1,0 +1,375 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 exact attention forward.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mine|reference]
+
+One step is one fused attention forward over the benchmark workload
+(default: B=2, H=16, N=8192, d=128, bf16, non-causal), with Q, K, V already
+resident in HBM.  The timed region holds exactly K launches, bracketed by a
+barrier and a device synchronisation; the inputs plus output (256 MiB) exceed
+the 129 MB L2, so steps do not reuse a warm cache.  Rank 0 prints one JSON line.
+
+Also measured in the same run (each in its own timed loop): the FP8 E4M3 path
+(attention alone, and preparation + attention) on the 8192-token FP8 workload,
+the other bf16 workloads, an end-to-end figure through the same C ABI with
+pinned host buffers (host-to-device copies of Q, K, V and device-to-host copies
+of O and lse inside the timed region), and the CPU oracle on a bounded sample
+of the workload.
+
+With --impl reference the float64 CPU oracle is timed instead (all host
+cores), on bounded samples of the same workload; only rank 0 works.
+Multi-GPU (torchrun): every rank runs its own replica of the workload (the
+path shards over independent (batch, head) slices with no exchange), value is
+the sum over ranks using the slowest rank's time.
+"""
+from __future__ import annotations
+
+import os
+
+# The CPU oracle runs in a thread pool; keep each BLAS call single-threaded so
+# the pool size is the number of cores actually used.
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+os.environ.setdefault("OMP_NUM_THREADS", "1")
+
+import argparse
+import concurrent.futures
+import json
+import math
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOP/s (bf16, FP8) and fraction of GB300 tensor peak"
+UNIT = "TFLOP/s"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16": p["bf16_tflops"],
+                "bf16_sustained": p["bf16_tflops_sustained"], "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.05)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append((float(f[1]), float(f[2]), f[5], f[6], f[7], f[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[2 + i] == "Active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws == 1:
+        return 0, 1, 0, None
+    import torch.distributed as dist
+    rank = int(os.environ["RANK"])
+    local = int(os.environ.get("LOCAL_RANK", rank))
+    return rank, ws, local, dist
+
+
+def _time_loop(fn, steps, stream):
+    import torch
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) / steps   # ms per step
+
+
+def _oracle_run(q, k, v, w, heads, threads):
+    """Time the float64 oracle on every query row of the listed (b, h) slices of
+    the workload's own inputs (CPU bf16 tensors); returns (seconds, flops)."""
+    import numpy as np
+    from oracle import attention as oa
+    f64 = lambda t: t.float().numpy().astype(np.float64)
+    rows = np.arange(w.N)
+    chunk = 256
+    jobs = [(b, h, rows[i:i + chunk]) for (b, h) in heads for i in range(0, w.N, chunk)]
+    vis = (rows + 1) if w.causal else np.full(rows.shape, w.N)
+    flops = 4.0 * w.d * float(vis.sum()) * len(heads)
+    slices = {(b, h): (f64(q[b, h]), f64(k[b, h]), f64(v[b, h])) for (b, h) in heads}
+    t0 = time.perf_counter()
+    with concurrent.futures.ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(lambda j: oa.three_pass_rows(*slices[(j[0], j[1])], w.scale, w.causal, j[2]),
+                    jobs))
+    return time.perf_counter() - t0, flops
+
+
+def run_reference(args):
+    from exact_attention_forward_fwd_gb300 import inputs
+    rank, ws, _, dist = _dist()
+    if rank != 0:
+        return
+    w = inputs.WORKLOADS[args.workload]
+    q, k, v = inputs.workload_inputs(w)
+    threads = os.cpu_count() or 1
+    all_heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+    per_step = 2
+    times, flops = [], 0.0
+    for i in range(args.warmup + args.steps):
+        heads = [all_heads[(per_step * i + j) % len(all_heads)] for j in range(per_step)]
+        t, f = _oracle_run(q, k, v, w, heads, threads)
+        if i >= args.warmup:
+            times.append(t)
+            flops += f
+    total = sum(times)
+    value = flops / total / 1e12
+    sample = (f"{per_step} (batch, head) slices x all {w.N} query rows of {w.name} per step "
+              f"(float64 three-pass oracle)")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N,
+                                         "d": w.d, "causal": w.causal},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def run_mine(args):
+    import torch
+    import exact_attention_forward_fwd_gb300 as ga
+    from exact_attention_forward_fwd_gb300 import build, inputs
+
+    rank, ws, local, dist = _dist()
+    torch.cuda.set_device(local)
+    if dist is not None:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    build.build()
+    ga.lib()
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    peaks = _peaks()
+    w = inputs.WORKLOADS[args.workload]
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    def max_over_ranks(x):
+        if dist is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    # ---------------------------------------------------------------- main
+    qh, kh, vh = inputs.workload_inputs(w)
+    q, k, v = qh.to(dev), kh.to(dev), vh.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(w.B, w.H, w.N, dtype=torch.float32, device=dev)
+    step = lambda: ga.attn_fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse)
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    with ClockSampler(local) as clk:
+        ms = _time_loop(step, args.steps, stream)
+    barrier()
+    if ga.device_status() != 0:
+        raise RuntimeError("kernel status word set during the benchmark")
+    ms = max_over_ranks(ms)
+    tflops_launch = w.flops / (ms * 1e-3) / 1e12
+    value = tflops_launch * ws
+
+    # ---------------------------------------------------------------- e2e
+    qp, kp, vp = (t.pin_memory() for t in (qh, kh, vh))
+    op = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    lp = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+
+    def e2e_step():
+        q.copy_(qp, non_blocking=True)
+        k.copy_(kp, non_blocking=True)
+        v.copy_(vp, non_blocking=True)
+        ga.attn_fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse)
+        op.copy_(o, non_blocking=True)
+        lp.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    barrier()
+    ms_e2e = max_over_ranks(_time_loop(e2e_step, max(3, args.steps // 2), stream))
+    barrier()
+    h2d = 3 * q.numel() * q.element_size()
+    d2h = o.numel() * o.element_size() + lse.numel() * 4
+
+    # ---------------------------------------------------------------- FP8
+    fp8 = None
+    if not args.no_extra:
+        wf = inputs.WORKLOADS["fp8_n8192_d128"]
+        fq, fk, fv = (t.to(dev) for t in inputs.workload_inputs(wf))
+        signs = inputs.make_signs(wf.H, wf.d, wf.seed).to(dev)
+        q8, sq = ga.fp8_prep(fq, signs)
+        k8, sk = ga.fp8_prep(fk, signs)
+        v8, sv = ga.fp8_prep(fv, None, transpose=True)
+        of = torch.empty_like(fq)
+        lf = torch.empty(wf.B, wf.H, wf.N, dtype=torch.float32, device=dev)
+        attn8 = lambda: ga.attn_fwd_fp8(q8, k8, v8, sq, sk, sv, causal=wf.causal, scale=wf.scale,
+                                        out=of, lse=lf)
+
+        def full8():
+            ga.fp8_prep(fq, signs, out=q8, scales=sq)
+            ga.fp8_prep(fk, signs, out=k8, scales=sk)
+            ga.fp8_prep(fv, None, transpose=True, out=v8, scales=sv)
+            attn8()
+
+        def prep8():
+            ga.fp8_prep(fq, signs, out=q8, scales=sq)
+            ga.fp8_prep(fk, signs, out=k8, scales=sk)
+            ga.fp8_prep(fv, None, transpose=True, out=v8, scales=sv)
+
+        for _ in range(args.warmup):
+            full8()
+        barrier()
+        ms8 = max_over_ranks(_time_loop(attn8, args.steps, stream))
+        ms8p = max_over_ranks(_time_loop(full8, args.steps, stream))
+        msprep = max_over_ranks(_time_loop(prep8, args.steps, stream))
+        barrier()
+        prep_bytes = 3 * fq.numel() * 2 + 3 * fq.numel() + 3 * sq.numel() * 4
+        t8 = wf.flops / (ms8 * 1e-3) / 1e12
+        fp8 = {"workload": wf.name, "attn_tflops": t8 * ws,
+               "attn_plus_prep_tflops": wf.flops / (ms8p * 1e-3) / 1e12 * ws,
+               "ms_attn": ms8, "ms_prep": msprep,
+               "roofline": {"bound": "tensor", "achieved": t8, "peak": 2 * peaks["bf16"],
+                            "unit": "TFLOP/s", "frac": t8 / (2 * peaks["bf16"]),
+                            "peak_note": "measured bf16 x 2 (nominal fp8/bf16 ratio)"},
+               "prep_roofline": {"bound": "hbm", "achieved": prep_bytes / (msprep * 1e-3) / 1e9,
+                                 "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                 "frac": prep_bytes / (msprep * 1e-3) / 1e9 / peaks["hbm_gbs"]}}
+        del fq, fk, fv, q8, k8, v8, of
+
+    # ------------------------------------------------------- other workloads
+    others = {}
+    if not args.no_extra:
+        for name in ("n8192_d128_causal", "n32768_d64_causal", "n2048_d128", "n2048_d128_causal"):
+            wo = inputs.WORKLOADS[name]
+            a, b, c = (t.to(dev) for t in inputs.workload_inputs(wo))
+            oo = torch.empty_like(a)
+            lo = torch.empty(wo.B, wo.H, wo.N, dtype=torch.float32, device=dev)
+            fn = lambda: ga.attn_fwd(a, b, c, causal=wo.causal, scale=wo.scale, out=oo, lse=lo)
+            for _ in range(args.warmup):
+                fn()
+            barrier()
+            mso = max_over_ranks(_time_loop(fn, args.steps, stream))
+            others[name] = {"tflops": wo.flops / (mso * 1e-3) / 1e12 * ws, "ms": mso}
+            del a, b, c, oo, lo
+        barrier()
+    if ga.device_status() != 0:
+        raise RuntimeError("kernel status word set during the benchmark")
+
+    # ---------------------------------------------------------- CPU baseline
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        threads = os.cpu_count() or 1
+        heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+        secs, flops = _oracle_run(qh, kh, vh, w, heads, threads)
+        cpu = {"value": flops / secs / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"the whole {w.name} workload, every row of every head (float64 "
+                         f"three-pass oracle, {secs:.1f} s)"}
+
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        try:
+            traffic = json.load(open(tpath)).get(f"attn_bf16_d{w.d}_{'causal' if w.causal else 'noncausal'}")
+        except Exception:
+            traffic = None
+    if rank == 0:
+        clocks = clk.summary()
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                       "causal": w.causal, "parallelism": f"replicas x{ws}",
+                       "l2": "inputs + output 256 MiB > 129 MB L2 (no flush)"},
+            "roofline": {"bound": "tensor", "achieved": tflops_launch, "peak": peaks["bf16"],
+                         "unit": "TFLOP/s", "frac": tflops_launch / peaks["bf16"],
+                         "traffic": traffic, "peak_source": peaks["source"] + " bf16 burst"},
+            "e2e": {"value": w.flops / (ms_e2e * 1e-3) / 1e12 * ws, "unit": UNIT,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
+            "gpu_launches": args.steps,
+            "clocks": {k2: clocks[k2] for k2 in ("sm_mhz", "sm_max_mhz", "reasons")},
+            "cpu_baseline": cpu,
+            "fp8": fp8,
+            "workloads": others,
+        }
+        print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
+    ap.add_argument("--workload", default="n8192_d128")
+    ap.add_argument("--no-extra", action="store_true", help="skip FP8 and other workloads")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)      # at least 3 untimed warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_mine(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,191 @@
+// C-ABI boundary: argument validation, TMA descriptor encoding, persistent
+// grid sizing and launch.  No allocation, no host synchronisation except in
+// attn_device_status().
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "attn.h"
+#include "attn_kernel.cuh"
+#include "launchers.h"
+#include "tmap.h"
+
+using namespace gb300;
+
+namespace {
+
+constexpr unsigned long long kDefaultTimeoutNs = 1000000000ull;   // 1 s per wait
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int units_for(int BH, int N) { return BH * ((N + 255) / 256); }
+
+// sm_103 (GB300) only: the library carries sm_103a code and nothing else.
+int device_check(int* num_sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+  int major = 0, minor = 0, sms = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  if (major != 10 || minor != 3) return ATTN_ERR_UNSUPPORTED;
+  *num_sms = sms;
+  return ATTN_OK;
+}
+
+int check_shape(int B, int H, int N, float scale, int causal) {
+  if (B < 1 || H < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * H > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  // Unit index (BH * pairs) and the flat output offsets stay in range.
+  if (static_cast<long long>(B) * H * ((N + 255) / 256) > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
+AttnParams base_params(void* o, float* lse, int BH, int N, float scale, int causal) {
+  AttnParams p{};
+  p.o = o;
+  p.lse = lse;
+  p.N = N;
+  p.BH = BH;
+  p.nkb = (N + 127) / 128;
+  p.npairs = (N + 255) / 256;
+  p.num_units = BH * p.npairs;
+  p.causal = causal;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.timeout_ns = kDefaultTimeoutNs;
+  return p;
+}
+
+int run_bf16(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+             int N, int d, float scale, int causal, int dtype, int* status,
+             unsigned long long timeout_ns, int skip_loads, cudaStream_t stream) {
+  if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
+  int rc = check_shape(B, H, N, scale, causal);
+  if (rc) return rc;
+  if (dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      (lse && !aligned(lse, 4)))
+    return ATTN_ERR_ALIGNMENT;
+  int sms = 0;
+  if ((rc = device_check(&sms))) return rc;
+  const int BH = B * H;
+  CUtensorMap mq, mk, mv;
+  const uint32_t box_inner = 64;   // 128-byte rows of the swizzle atom
+  if (!encode_map_3d(&mq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, N, BH, box_inner, 128) ||
+      !encode_map_3d(&mk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, N, BH, box_inner, 128) ||
+      !encode_map_3d(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, N, BH, box_inner, 128))
+    return ATTN_ERR_CUDA;
+  AttnParams p = base_params(o, lse, BH, N, scale, causal);
+  p.status = status;
+  p.timeout_ns = timeout_ns;
+  p.skip_load = skip_loads;
+  const int grid = p.num_units < sms ? p.num_units : sms;
+  cudaError_t e = (d == 64) ? launch_attn_bf16_d64(mq, mk, mv, p, grid, stream)
+                            : launch_attn_bf16_d128(mq, mk, mv, p, grid, stream);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+             int d, float scale, int causal, int dtype, attn_stream_t stream) {
+  return run_bf16(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, nullptr, kDefaultTimeoutNs,
+                  0, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int attn_fwd_debug(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                   int N, int d, float scale, int causal, int* dev_status,
+                   unsigned long long timeout_ns, int skip_loads, attn_stream_t stream) {
+  if (!dev_status || !aligned(dev_status, 4) || timeout_ns == 0 || skip_loads < 0)
+    return ATTN_ERR_INVALID_ARG;
+  return run_bf16(q, k, v, o, lse, B, H, N, d, scale, causal, ATTN_BF16, dev_status, timeout_ns,
+                  skip_loads, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int attn_fp8_prep(const void* x, void* x8, float* block_scale, const signed char* signs, int B,
+                  int H, int N, int d, int transpose_out, attn_stream_t stream) {
+  if (!x || !x8 || !block_scale) return ATTN_ERR_INVALID_ARG;
+  int rc = check_shape(B, H, N, 1.0f, 0);
+  if (rc) return rc;
+  if (transpose_out != 0 && transpose_out != 1) return ATTN_ERR_INVALID_ARG;
+  if (d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned(x, 16) || !aligned(x8, 16) || !aligned(block_scale, 4) || (signs && !aligned(signs, 4)))
+    return ATTN_ERR_ALIGNMENT;
+  int sms = 0;
+  if ((rc = device_check(&sms))) return rc;
+  cudaError_t e = launch_fp8_prep(x, x8, block_scale, signs, B * H, H, N, transpose_out,
+                                  reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int attn_fwd_fp8(const void* q8, const void* k8, const void* v8t, const float* q_scale,
+                 const float* k_scale, const float* v_scale, void* o, float* lse, int B, int H,
+                 int N, int d, float scale, int causal, attn_stream_t stream) {
+  if (!q8 || !k8 || !v8t || !q_scale || !k_scale || !v_scale || !o) return ATTN_ERR_INVALID_ARG;
+  int rc = check_shape(B, H, N, scale, causal);
+  if (rc) return rc;
+  if (d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned(q8, 16) || !aligned(k8, 16) || !aligned(v8t, 16) || !aligned(o, 16) ||
+      !aligned(q_scale, 4) || !aligned(k_scale, 4) || !aligned(v_scale, 4) ||
+      (lse && !aligned(lse, 4)))
+    return ATTN_ERR_ALIGNMENT;
+  int sms = 0;
+  if ((rc = device_check(&sms))) return rc;
+  const int BH = B * H;
+  const int Npad = ((N + 127) / 128) * 128;
+  CUtensorMap mq, mk, mv;
+  if (!encode_map_3d(&mq, q8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, d, N, BH, 128, 128) ||
+      !encode_map_3d(&mk, k8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, d, N, BH, 128, 128) ||
+      !encode_map_3d(&mv, v8t, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Npad, d, BH, 128, 128))
+    return ATTN_ERR_CUDA;
+  AttnParams p = base_params(o, lse, BH, N, scale, causal);
+  p.q_scale = q_scale;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  const int grid = p.num_units < sms ? p.num_units : sms;
+  cudaError_t e = launch_attn_fp8_d128(mq, mk, mv, p, grid, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int attn_device_status(int clear) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_ERR_CUDA;
+  int out = ATTN_OK;
+  const int s[3] = {status_attn_bf16_d64(clear != 0), status_attn_bf16_d128(clear != 0),
+                    status_attn_fp8_d128(clear != 0)};
+  for (int i = 0; i < 3; ++i)
+    if (s[i] != 0 && out == ATTN_OK) out = s[i];
+  return out;
+}
+
+int attn_num_units(int B, int H, int N) {
+  if (B < 1 || H < 1 || N < 1) return 0;
+  return units_for(B * H, N);
+}
+
+int attn_grid_size(int B, int H, int N, int num_sms) {
+  const int u = attn_num_units(B, H, N);
+  if (num_sms < 1) return 0;
+  return u < num_sms ? u : num_sms;
+}
+
+const char* attn_status_str(int status) {
+  switch (status) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported head dim, dtype or device";
+    case ATTN_ERR_ALIGNMENT: return "tensor base address not 16-byte aligned";
+    case ATTN_ERR_CUDA: return "CUDA runtime or driver call failed";
+    case ATTN_ERR_TIMEOUT: return "a pipeline wait inside the kernel ran out of time";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,570 @@
+// Fused exact attention forward for sm_103a: O = softmax(scale * Q K^T [+causal]) V
+// and lse = log sum exp(scale * Q K^T) per row, without writing the N x N
+// score matrix anywhere.
+//
+// Method (as described on "Learn: The Memory Wall & FlashAttention", section
+// 5.1, and "4.3 FlashAttention 2 & 3", sections "Edit 1/2/3" and
+// "FlashAttention-3: exploiting Hopper"):
+//   * tiled over query blocks, streaming over key/value blocks;
+//   * online softmax: running max m, running denominator l, unnormalised
+//     accumulator O~ rescaled by alpha = exp(m_old - m_new), one final O~ / l;
+//   * causal: key blocks strictly in the future are skipped, the diagonal
+//     blocks are masked element-wise (key > query -> -inf);
+//   * producer/consumer warp specialisation over a shared-memory ring with
+//     mbarriers; the score MMA of the next block overlaps the softmax of the
+//     current one.
+//
+// Blackwell mapping (this file's own design):
+//   * one persistent CTA per SM; a work unit is (batch*head, pair of 128-row
+//     query tiles); both tiles share every K/V block loaded;
+//   * warps 0-3 / 4-7: softmax of tile 0 / tile 1, one thread per query row,
+//     reading S from tensor memory (TMEM) and writing P back over it;
+//   * warp 8: TMA loads of Q (once per unit) and of K, V blocks into the ring;
+//   * warp 9: allocates TMEM and issues every tcgen05.mma from one thread:
+//       S_t = Q_t K_j^T  (SS, both operands K-major in shared memory)
+//       O_t += P_t V_j   (TS, P from TMEM, V from shared memory)
+//     ordered PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), ... so the tensor pipe
+//     always has the other tile's work while one tile's softmax runs;
+//   * TMEM columns: S/P tile 0 [0,128), S/P tile 1 [128,256), O tile 0
+//     [256,256+D), O tile 1 [256+D, 256+2D);
+//   * scale folded into exp2: p = 2^(s * scale*log2(e) - m), m kept in the
+//     same base-2 units;
+//   * conditional rescaling: the reference max used for the exponentials is
+//     only moved (and O~, l rescaled) when the block max exceeds it by more
+//     than tau (base-2 units).  Numerator and denominator always share the
+//     same reference, so the result stays exact; p <= 2^tau.
+//   * because every tcgen05.commit tracks all earlier MMAs of the issuing
+//     thread, the arrival of S_t(j) also proves O_t += P_t(j-1) V(j-1) is
+//     complete: a rescale of O~ right after waiting for S_t(j) is race-free.
+//
+// FP8 variant (E4M3 operands, f32 accumulation): per-128-row block scales of
+// Q, K, V ("FlashAttention-3: How Warp Specialization ...", section 4); the
+// score scale of block j is folded into the exp2 factor, P is quantised to
+// E4M3 as p * 256 * s_V(j) / max_j s_V(j) (tau = 0 so p <= 1), which folds
+// V's per-block scale into P, and the epilogue divides by 256 * l / max s_V.
+// V arrives transposed ([d][N], keys contiguous) so both MMAs read K-major
+// operands.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace gb300 {
+
+enum : int { kStatusOk = 0, kStatusTimeout = -5 };
+
+struct AttnParams {
+  void* o;               // bf16 [BH][N][D]
+  float* lse;            // fp32 [BH][N] or null
+  const float* q_scale;  // FP8 only: [BH][nqb]
+  const float* k_scale;  // FP8 only: [BH][nkb]
+  const float* v_scale;  // FP8 only: [BH][nkb]
+  int* status;           // device status word, or null for the library's own word
+  int N;                 // sequence length (queries == keys)
+  int BH;                // batch * heads
+  int nkb;               // ceil(N / 128): key blocks (and 128-row query tiles)
+  int npairs;            // ceil(N / 256): query-tile pairs per head
+  int num_units;         // BH * npairs
+  int causal;
+  float scale_log2;      // scale * log2(e)
+  unsigned long long timeout_ns;
+  int skip_load;         // test hook: when > 0, the load warp stops after that many K/V loads
+};
+
+template <int D, bool FP8>
+struct KCfg {
+  static_assert(D == 64 || D == 128, "head dim 64 or 128");
+  static_assert(!FP8 || D == 128, "FP8 path: head dim 128");
+  static constexpr int kRowBytes = FP8 ? D : 2 * D;        // one Q/K row in bytes
+  static constexpr int kSlabs = kRowBytes / 128;           // 128-byte column slabs per tile
+  static constexpr int kTileBytes = 128 * kRowBytes;       // 128-row tile (V / V^T tile the same)
+  static constexpr int kStages = (kTileBytes == 32768) ? 4 : 8;
+  static constexpr int kSmemBytes = (2 + kStages) * kTileBytes + 1024;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr int kThreads = 320;
+  static constexpr float kTau = FP8 ? 0.0f : 8.0f;
+  static constexpr int kSKSteps = FP8 ? D / 32 : D / 16;  // k-steps of S = Q K^T
+  static constexpr int kPVSteps = FP8 ? 4 : 8;            // k-steps of O += P V (128 keys)
+  static constexpr uint32_t kIdescS =
+      make_idesc(128, 128, FP8 ? 0u : 1u, FP8 ? 0u : 1u, false, false);
+  static constexpr uint32_t kIdescPV =
+      make_idesc(128, D, FP8 ? 0u : 1u, FP8 ? 0u : 1u, false, !FP8);
+};
+
+struct SmemCtl {
+  uint64_t kv_full[8];
+  uint64_t kv_empty[8];
+  uint64_t q_full[2];
+  uint64_t q_empty[2];
+  uint64_t s_full[2];
+  uint64_t p_ready[2];
+  uint64_t o_final[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+// Status word of launches that pass no status pointer (one per translation
+// unit; read back by the host through cudaMemcpyFromSymbol).
+static __device__ int g_attn_status;
+
+struct WaitCtx {
+  SmemCtl* ctl;
+  int* status;
+  unsigned long long timeout_ns;
+};
+
+// Bounded wait on an mbarrier phase.  Returns false if the CTA was told to
+// abort or the limit ran out (which sets the abort flag and the status word).
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const WaitCtx& wc,
+                                             bool honour_abort = true) {
+  SmemCtl* ctl = wc.ctl;
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (honour_abort && *reinterpret_cast<volatile int*>(&ctl->abort_flag)) return false;
+    if (global_timer_ns() - t0 > wc.timeout_ns) {
+      *reinterpret_cast<volatile int*>(&ctl->abort_flag) = 1;
+      atomicCAS(wc.status, kStatusOk, kStatusTimeout);
+      return false;
+    }
+  }
+}
+
+struct Unit {
+  int bh, pair, nblocks;
+};
+
+// Work unit u -> (head, query-tile pair, key blocks to visit).  Non-causal:
+// consecutive units walk the pairs of one head (K/V of a head stay hot in L2).
+// Causal: longest first -- all heads' last pair, then the one before, ...
+__device__ __forceinline__ Unit unit_of(int u, const AttnParams& p) {
+  Unit w;
+  if (p.causal) {
+    const int r = u / p.BH;
+    w.bh = u - r * p.BH;
+    w.pair = p.npairs - 1 - r;
+    w.nblocks = min(p.nkb, 2 * w.pair + 2);
+  } else {
+    w.bh = u / p.npairs;
+    w.pair = u - w.bh * p.npairs;
+    w.nblocks = p.nkb;
+  }
+  return w;
+}
+
+template <int D, bool FP8>
+__global__ void __launch_bounds__(320, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+  using C = KCfg<D, FP8>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ SmemCtl ctl;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sQ = smem_addr(smem);                         // Q tile 0, Q tile 1
+  const uint32_t sKV = sQ + 2 * C::kTileBytes;                 // ring of K / V tiles
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  auto bar = [&](uint64_t& b) { return smem_addr(&b); };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(bar(ctl.kv_full[s]), 1);
+      mbar_init(bar(ctl.kv_empty[s]), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(ctl.q_full[t]), 1);
+      mbar_init(bar(ctl.q_empty[t]), 1);
+      mbar_init(bar(ctl.s_full[t]), 1);
+      mbar_init(bar(ctl.p_ready[t]), 128);
+      mbar_init(bar(ctl.o_final[t]), 1);
+    }
+    mbar_init(bar(ctl.drain), 1);
+    ctl.abort_flag = 0;
+    fence_mbarrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_addr(&ctl.tmem_base), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl.tmem_base;
+  const WaitCtx wc{&ctl, p.status ? p.status : &g_attn_status, p.timeout_ns};
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tensormap(&tmQ);
+      prefetch_tensormap(&tmK);
+      prefetch_tensormap(&tmV);
+      const uint64_t pol_kv = l2_policy_evict_last();
+      const uint64_t pol_q = l2_policy_evict_first();
+      uint32_t item = 0;        // K/V ring items issued
+      uint32_t uit = 0;         // units started
+      uint32_t qn[2] = {0, 0};  // Q tiles issued per tile slot
+      bool ok = true;
+      int loads = 0;
+      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uit) {
+        const Unit w = unit_of(u, p);
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (uit > 0) ok = wait_bounded(bar(ctl.q_empty[t]), (uit - 1) & 1, wc);
+          if (!ok) break;
+          mbar_arrive_expect_tx(bar(ctl.q_full[t]), C::kTileBytes);
+          ++qn[t];
+          const int row0 = w.pair * 256 + t * 128;
+          for (int s = 0; s < C::kSlabs; ++s)
+            tma_load_3d_hint(sQ + t * C::kTileBytes + s * 16384, &tmQ, bar(ctl.q_full[t]),
+                             s * (FP8 ? 128 : 64), row0, w.bh, pol_q);
+        }
+        for (int j = 0; j < w.nblocks && ok; ++j) {
+          for (int kv = 0; kv < 2 && ok; ++kv, ++item) {
+            if (p.skip_load > 0 && loads >= p.skip_load) break;   // test hook only
+            const uint32_t slot = item % C::kStages;
+            const uint32_t ph = (item / C::kStages) & 1;
+            ok = wait_bounded(bar(ctl.kv_empty[slot]), ph ^ 1, wc);
+            if (!ok) break;
+            const uint32_t dst = sKV + slot * C::kTileBytes;
+            mbar_arrive_expect_tx(bar(ctl.kv_full[slot]), C::kTileBytes);
+            if (kv == 0) {
+              for (int s = 0; s < C::kSlabs; ++s)
+                tma_load_3d_hint(dst + s * 16384, &tmK, bar(ctl.kv_full[slot]),
+                                 s * (FP8 ? 128 : 64), j * 128, w.bh, pol_kv);
+            } else if (FP8) {
+              // V^T [BH][D][Npad]: one 128-key x D tile
+              tma_load_3d_hint(dst, &tmV, bar(ctl.kv_full[slot]), j * 128, 0, w.bh, pol_kv);
+            } else {
+              for (int s = 0; s < C::kSlabs; ++s)
+                tma_load_3d_hint(dst + s * 16384, &tmV, bar(ctl.kv_full[slot]), s * 64, j * 128,
+                                 w.bh, pol_kv);
+            }
+            ++loads;
+          }
+        }
+      }
+      // Let every copy this warp started land before the CTA can exit.
+      const uint32_t issued = item;
+      for (uint32_t s = 0; s < (uint32_t)C::kStages && s < issued; ++s) {
+        const uint32_t last = s + ((issued - 1 - s) / C::kStages) * C::kStages;
+        wait_bounded(bar(ctl.kv_full[s]), (last / C::kStages) & 1, wc, false);
+      }
+      for (int t = 0; t < 2; ++t)
+        if (qn[t] > 0) wait_bounded(bar(ctl.q_full[t]), (qn[t] - 1) & 1, wc, false);
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t item = 0, uit = 0, pr[2] = {0, 0};
+      bool ok = true;
+      auto s_mma = [&](int t, uint32_t kslot) {
+        const uint32_t a0 = sQ + t * C::kTileBytes;
+        const uint32_t b0 = sKV + kslot * C::kTileBytes;
+#pragma unroll
+        for (int k = 0; k < C::kSKSteps; ++k) {
+          const uint32_t off = FP8 ? k * 32 : (k >> 2) * 16384 + (k & 3) * 32;
+          const uint64_t da = make_smem_desc(a0 + off, 16, 1024, kSwizzle128B);
+          const uint64_t db = make_smem_desc(b0 + off, 16, 1024, kSwizzle128B);
+          if (FP8)
+            mma_f8_ss(tmem + 128 * t, da, db, C::kIdescS, k > 0);
+          else
+            mma_f16_ss(tmem + 128 * t, da, db, C::kIdescS, k > 0);
+        }
+      };
+      auto pv_mma = [&](int t, uint32_t vslot, bool acc) {
+        const uint32_t b0 = sKV + vslot * C::kTileBytes;
+#pragma unroll
+        for (int k = 0; k < C::kPVSteps; ++k) {
+          const uint32_t a = tmem + 128 * t + k * 8;
+          if (FP8) {
+            const uint64_t db = make_smem_desc(b0 + k * 32, 16, 1024, kSwizzle128B);
+            mma_f8_ts(tmem + 256 + D * t, a, db, C::kIdescPV, (acc || k > 0) ? 1u : 0u);
+          } else {
+            const uint64_t db = make_smem_desc(b0 + k * 2048, 16384, 1024, kSwizzle128B);
+            mma_f16_ts(tmem + 256 + D * t, a, db, C::kIdescPV, (acc || k > 0) ? 1u : 0u);
+          }
+        }
+      };
+      auto wait_item = [&](uint32_t it) {
+        return wait_bounded(bar(ctl.kv_full[it % C::kStages]), (it / C::kStages) & 1, wc);
+      };
+      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uit) {
+        const Unit w = unit_of(u, p);
+        const int J = w.nblocks;
+        ok = wait_bounded(bar(ctl.q_full[0]), uit & 1, wc) &&
+             wait_bounded(bar(ctl.q_full[1]), uit & 1, wc);
+        if (!ok) break;
+        const uint32_t base = item;            // K_j = base + 2j, V_j = base + 2j + 1
+        item += 2 * J;
+        if (!(ok = wait_item(base))) break;
+        tc_fence_after();
+        s_mma(0, base % C::kStages);
+        mma_commit(bar(ctl.s_full[0]));
+        s_mma(1, base % C::kStages);
+        mma_commit(bar(ctl.s_full[1]));
+        mma_commit(bar(ctl.kv_empty[base % C::kStages]));
+        if (J == 1) {
+          mma_commit(bar(ctl.q_empty[0]));
+          mma_commit(bar(ctl.q_empty[1]));
+        }
+        for (int j = 0; j < J && ok; ++j) {
+          const uint32_t iv = base + 2 * j + 1, ik = base + 2 * j + 2;
+          const uint32_t vslot = iv % C::kStages, kslot = ik % C::kStages;
+          if (!(ok = wait_item(iv))) break;
+          if (!(ok = wait_bounded(bar(ctl.p_ready[0]), pr[0]++ & 1, wc))) break;
+          tc_fence_after();
+          pv_mma(0, vslot, j > 0);
+          if (j == J - 1) mma_commit(bar(ctl.o_final[0]));
+          if (j + 1 < J) {
+            if (!(ok = wait_item(ik))) break;
+            tc_fence_after();
+            s_mma(0, kslot);
+            mma_commit(bar(ctl.s_full[0]));
+          }
+          if (!(ok = wait_bounded(bar(ctl.p_ready[1]), pr[1]++ & 1, wc))) break;
+          tc_fence_after();
+          pv_mma(1, vslot, j > 0);
+          mma_commit(bar(ctl.kv_empty[vslot]));
+          if (j == J - 1) mma_commit(bar(ctl.o_final[1]));
+          if (j + 1 < J) {
+            s_mma(1, kslot);
+            mma_commit(bar(ctl.s_full[1]));
+            mma_commit(bar(ctl.kv_empty[kslot]));
+            if (j + 2 == J) {
+              mma_commit(bar(ctl.q_empty[0]));
+              mma_commit(bar(ctl.q_empty[1]));
+            }
+          }
+        }
+      }
+      // Every MMA issued must finish before TMEM is released.
+      mma_commit(bar(ctl.drain));
+      wait_bounded(bar(ctl.drain), 0, wc, false);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int t = warp >> 2;                 // query tile of the pair
+    const int wq = warp & 3;                 // TMEM lane quarter
+    const int r = wq * 32 + lane;            // row within the tile
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_off + 128 * t;
+    const uint32_t tO = tmem + lane_off + 256 + D * t;
+    const float tau = C::kTau;
+    const float NEG_INF = __int_as_float(0xff800000);
+    uint32_t sit = 0, uit = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uit) {
+      const Unit w = unit_of(u, p);
+      const int row = w.pair * 256 + t * 128 + r;
+      const int lim_row = p.causal ? min(row, p.N - 1) : p.N - 1;   // last visible key
+      float m_ref = NEG_INF, ell = 0.0f;   // reference max (base 2), sum of f32 p
+      float ell_r = 0.0f;                   // sum of p as rounded into P (bf16 path)
+      float q_s = 1.0f, v_smax = 1.0f;
+      if (FP8) {
+        const int qb = w.pair * 2 + t;
+        q_s = (qb < p.nkb) ? __ldg(p.q_scale + (size_t)w.bh * p.nkb + qb) : 1.0f;
+        float mx = 0.0f;
+        for (int b = lane; b < p.nkb; b += 32) mx = fmaxf(mx, __ldg(p.v_scale + (size_t)w.bh * p.nkb + b));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        v_smax = mx;
+      }
+      for (int j = 0; j < w.nblocks; ++j) {
+        ok = wait_bounded(bar(ctl.s_full[t]), sit++ & 1, wc);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t sr[128];
+        tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+        tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+        tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
+        tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
+        tmem_wait_ld();
+        reg_fence(sr);
+        float x[128];
+#pragma unroll
+        for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(sr[c]);
+        float cj = p.scale_log2;
+        float v_fold = 1.0f;
+        if (FP8) {
+          cj *= q_s * __ldg(p.k_scale + (size_t)w.bh * p.nkb + j);
+          v_fold = 256.0f * __ldg(p.v_scale + (size_t)w.bh * p.nkb + j) / v_smax;
+        }
+        const int lim = lim_row - j * 128;    // columns > lim are invisible
+        if (lim < 127) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c) x[c] = (c > lim) ? NEG_INF : x[c];
+        }
+        float m0 = x[0], m1 = x[1], m2 = x[2], m3 = x[3];
+#pragma unroll
+        for (int c = 4; c < 128; c += 8) {
+          m0 = max3(m0, x[c], x[c + 1]);
+          m1 = max3(m1, x[c + 2], x[c + 3]);
+          m2 = max3(m2, x[c + 4], x[c + 5]);
+          m3 = max3(m3, x[c + 6], x[c + 7]);
+        }
+        const float mx = max3(m0, m1, fmaxf(m2, m3));
+        const float m_blk = mx * cj;
+        const bool need = m_blk > m_ref + tau;
+        const float m_new = need ? m_blk : m_ref;
+        const float alpha = need ? ex2_approx(m_ref - m_new) : 1.0f;   // 0 when m_ref = -inf
+        if (j > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll 1
+          for (int cc = 0; cc < D; cc += 32) {
+            uint32_t orow[32];
+            tmem_ld32(tO + cc, orow);
+            tmem_wait_ld();
+            reg_fence(orow);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) orow[i] = __float_as_uint(__uint_as_float(orow[i]) * alpha);
+            tmem_st32(tO + cc, orow);
+          }
+        }
+        ell *= alpha;
+        ell_r *= alpha;
+        m_ref = m_new;
+        const float m_use = (m_ref == NEG_INF) ? 0.0f : m_ref;
+        __syncwarp();   // tcgen05.st is warp-collective: reconverge after the mask branch
+        if (FP8) {
+          float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+          uint32_t pk[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float p0 = ex2_approx(fmaf(x[4 * i], cj, -m_use));
+            const float p1 = ex2_approx(fmaf(x[4 * i + 1], cj, -m_use));
+            const float p2 = ex2_approx(fmaf(x[4 * i + 2], cj, -m_use));
+            const float p3 = ex2_approx(fmaf(x[4 * i + 3], cj, -m_use));
+            l0 += p0;
+            l1 += p1;
+            l2 += p2;
+            l3 += p3;
+            pk[i] = pack_e4m3x4(p0 * v_fold, p1 * v_fold, p2 * v_fold, p3 * v_fold);
+          }
+          ell += (l0 + l1) + (l2 + l3);
+          tmem_st32(tS, pk);
+        } else {
+          // p = 2^(s*c - m) in pairs.  P is rounded to bf16 for the PV MMA; the
+          // sum of exactly those rounded values (l~) normalises O, so numerator
+          // and denominator use the same weights, while the sum of the f32
+          // values (l) gives the logsumexp.
+          const uint64_t c2 = f32x2_pack(cj, cj);
+          const uint64_t nm2 = f32x2_pack(-m_use, -m_use);
+          uint64_t ex0 = 0, ex1 = 0;   // (0.f, 0.f)
+          float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
+          uint32_t pk[64];
+#pragma unroll
+          for (int i = 0; i < 64; ++i) {
+            float t0, t1;
+            f32x2_unpack(f32x2_fma(f32x2_pack(x[2 * i], x[2 * i + 1]), c2, nm2), t0, t1);
+            const float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
+            const uint32_t pb = pack_bf16x2(p0, p1);
+            pk[i] = pb;
+            const uint64_t e = f32x2_pack(p0, p1);
+            if (i & 1) {
+              r2 = add_bf16_lo(pb, r2);
+              r3 = add_bf16_hi(pb, r3);
+              ex1 = f32x2_add(ex1, e);
+            } else {
+              r0 = add_bf16_lo(pb, r0);
+              r1 = add_bf16_hi(pb, r1);
+              ex0 = f32x2_add(ex0, e);
+            }
+          }
+          float b0, b1;
+          f32x2_unpack(f32x2_add(ex0, ex1), b0, b1);
+          ell_r += (r0 + r1) + (r2 + r3);
+          ell += b0 + b1;
+          tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+          tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(ctl.p_ready[t]));
+      }
+      if (!ok) break;
+      // ---------------------------------------------------------- epilogue
+      ok = wait_bounded(bar(ctl.o_final[t]), uit & 1, wc);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      float inv;
+      if (FP8)
+        inv = (ell > 0.0f) ? v_smax * (1.0f / 256.0f) / ell : 0.0f;
+      else
+        inv = (ell_r > 0.0f) ? 1.0f / ell_r : 0.0f;
+      const bool live = row < p.N;
+      uint16_t* orow_g = reinterpret_cast<uint16_t*>(p.o) + ((size_t)w.bh * p.N + row) * D;
+#pragma unroll 1
+      for (int cc = 0; cc < D; cc += 32) {
+        uint32_t ov[32];
+        __syncwarp();
+        tmem_ld32(tO + cc, ov);
+        tmem_wait_ld();
+        reg_fence(ov);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv, __uint_as_float(ov[2 * i + 1]) * inv);
+        if (live) {
+          uint4* dst = reinterpret_cast<uint4*>(orow_g + cc);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
+      }
+      if (live && p.lse != nullptr) {
+        const float l2e = (ell > 0.0f) ? (m_ref + __log2f(ell)) * 0.69314718055994531f : NEG_INF;
+        p.lse[(size_t)w.bh * p.N + row] = l2e;
+      }
+      // The next unit's first P arrive (after this epilogue) releases O_t.
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 9) tmem_dealloc(tmem, C::kTmemCols);
+}
+
+}  // namespace gb300
+
+namespace gb300 {
+
+// Host-side launch of one instantiation (defined in this header so that each
+// translation unit instantiates exactly one configuration).
+template <int D, bool FP8>
+cudaError_t launch_attn(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                        const AttnParams& p, int grid, cudaStream_t stream) {
+  using C = KCfg<D, FP8>;
+  auto kern = attn_fwd_kernel<D, FP8>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, kern, q, k, v, p);
+}
+
+// Status word of this translation unit's kernels.
+inline int read_tu_status(bool clear) {
+  int s = 0;
+  if (cudaMemcpyFromSymbol(&s, g_attn_status, sizeof(int)) != cudaSuccess) return -4;
+  if (clear && s != 0) {
+    int z = 0;
+    if (cudaMemcpyToSymbol(g_attn_status, &z, sizeof(int)) != cudaSuccess) return -4;
+  }
+  return s;
+}
+
+}  // namespace gb300

@@ -1,0 +1,156 @@
+// FP8 E4M3 operand preparation (memory-bound): optional incoherent-processing
+// rotation of each row by H_128 diag(signs) (fast Walsh-Hadamard transform),
+// then per block of 128 rows: s = amax / 448 (1 for an all-zero block) and
+// codes = E4M3_rn_satfinite(x / s).
+//
+// Sources: "4.3 FlashAttention 2 & 3: Work Partitioning, Warp Specialization &
+// FP8", section "Incoherent processing: rotate away the outliers" (M = H D
+// applied as x M, orthonormal Sylvester H, O(d log d) fast transform, s =
+// amax / 448); "FlashAttention-3: How Warp Specialization, Asynchronous TMA
+// Tiling, and FP8 Hardware Acceleration Scale Attention on Hopper GPUs",
+// section 4 (one scale per block of each operand).
+//
+// One CTA per (batch*head, 128-row block), 8 warps x 16 rows; each lane owns
+// 4 consecutive columns of a 128-column row.  Butterfly stages of half-width
+// 1 and 2 stay inside a lane; stages 4..64 exchange with lane ^ (h / 4).
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "launchers.h"
+#include "ptx.cuh"
+
+namespace gb300 {
+
+namespace {
+
+constexpr int kRows = 128;
+constexpr int kD = 128;
+constexpr float kInvSqrtD = 0.08838834764831845f;   // 1 / sqrt(128)
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+template <bool ROTATE, bool TRANSPOSE>
+__global__ void __launch_bounds__(256) fp8_prep_kernel(const uint16_t* __restrict__ x,
+                                                       uint8_t* __restrict__ x8,
+                                                       float* __restrict__ scales,
+                                                       const int8_t* __restrict__ signs, int H,
+                                                       int N, int nblk, int Npad) {
+  __shared__ float warp_max[8];
+  __shared__ __align__(16) uint8_t tile[TRANSPOSE ? kRows * kD : 16];
+  const int blk = blockIdx.x % nblk;
+  const int bh = blockIdx.x / nblk;
+  const int h = bh % H;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  float sg[4] = {1.f, 1.f, 1.f, 1.f};
+  if (ROTATE) {
+    const uint32_t s4 = *reinterpret_cast<const uint32_t*>(signs + (size_t)h * kD + 4 * lane);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) sg[e] = static_cast<float>(static_cast<int8_t>((s4 >> (8 * e)) & 0xFF)) * kInvSqrtD;
+  }
+
+  float v[16][4];
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int r = blk * kRows + warp * 16 + i;
+    float a[4] = {0.f, 0.f, 0.f, 0.f};
+    if (r < N) {
+      const uint2 raw = *reinterpret_cast<const uint2*>(x + ((size_t)bh * N + r) * kD + 4 * lane);
+      a[0] = bf16_to_f32(raw.x & 0xFFFF);
+      a[1] = bf16_to_f32(raw.x >> 16);
+      a[2] = bf16_to_f32(raw.y & 0xFFFF);
+      a[3] = bf16_to_f32(raw.y >> 16);
+    }
+    if (ROTATE) {
+      // half-width 1: (0,1), (2,3)
+      float b0 = a[0] + a[1], b1 = a[0] - a[1], b2 = a[2] + a[3], b3 = a[2] - a[3];
+      // half-width 2: (0,2), (1,3)
+      a[0] = b0 + b2;
+      a[1] = b1 + b3;
+      a[2] = b0 - b2;
+      a[3] = b1 - b3;
+#pragma unroll
+      for (int m = 1; m < 32; m <<= 1) {   // half-width 4m across lanes
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float o = __shfl_xor_sync(0xffffffffu, a[e], m);
+          a[e] = upper ? (o - a[e]) : (a[e] + o);
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) a[e] *= sg[e];
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      v[i][e] = a[e];
+      amax = fmaxf(amax, fabsf(a[e]));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if (lane == 0) warp_max[warp] = amax;
+  __syncthreads();
+  float bmax = warp_max[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) bmax = fmaxf(bmax, warp_max[w]);
+  const float s = (bmax > 0.f) ? __fdiv_rn(bmax, 448.0f) : 1.0f;
+  if (threadIdx.x == 0) scales[(size_t)bh * nblk + blk] = s;
+
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int rl = warp * 16 + i;
+    const int r = blk * kRows + rl;
+    const uint32_t code = pack_e4m3x4(__fdiv_rn(v[i][0], s), __fdiv_rn(v[i][1], s),
+                                      __fdiv_rn(v[i][2], s), __fdiv_rn(v[i][3], s));
+    if (TRANSPOSE) {
+      *reinterpret_cast<uint32_t*>(tile + rl * kD + 4 * lane) = code;
+    } else if (r < N) {
+      *reinterpret_cast<uint32_t*>(x8 + ((size_t)bh * N + r) * kD + 4 * lane) = code;
+    }
+  }
+  if (TRANSPOSE) {
+    __syncthreads();
+    // Output row c (a head-dim column) holds this block's 128 keys, contiguous.
+    const int c = threadIdx.x >> 1;
+    const int k0 = (threadIdx.x & 1) * 64;
+    uint32_t w[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      uint32_t acc = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc |= static_cast<uint32_t>(tile[(k0 + 4 * q + e) * kD + c]) << (8 * e);
+      w[q] = acc;
+    }
+    uint4* dst = reinterpret_cast<uint4*>(x8 + ((size_t)bh * kD + c) * Npad + (size_t)blk * kRows + k0);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_fp8_prep(const void* x, void* x8, float* scales, const signed char* signs,
+                            int BH, int H, int N, int transpose_out, cudaStream_t stream) {
+  const int nblk = (N + kRows - 1) / kRows;
+  const int Npad = nblk * kRows;
+  const dim3 grid(static_cast<unsigned>(BH) * nblk), block(256);
+  const auto* xs = static_cast<const uint16_t*>(x);
+  auto* xo = static_cast<uint8_t*>(x8);
+  const auto* sg = reinterpret_cast<const int8_t*>(signs);
+  if (signs && transpose_out)
+    fp8_prep_kernel<true, true><<<grid, block, 0, stream>>>(xs, xo, scales, sg, H, N, nblk, Npad);
+  else if (signs)
+    fp8_prep_kernel<true, false><<<grid, block, 0, stream>>>(xs, xo, scales, sg, H, N, nblk, Npad);
+  else if (transpose_out)
+    fp8_prep_kernel<false, true><<<grid, block, 0, stream>>>(xs, xo, scales, sg, H, N, nblk, Npad);
+  else
+    fp8_prep_kernel<false, false><<<grid, block, 0, stream>>>(xs, xo, scales, sg, H, N, nblk, Npad);
+  return cudaGetLastError();
+}
+
+}  // namespace gb300

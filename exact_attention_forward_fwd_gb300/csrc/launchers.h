@@ -1,0 +1,26 @@
+// Entry points of the per-configuration kernel translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace gb300 {
+
+struct AttnParams;
+
+cudaError_t launch_attn_bf16_d64(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                                 const AttnParams&, int grid, cudaStream_t);
+cudaError_t launch_attn_bf16_d128(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                                  const AttnParams&, int grid, cudaStream_t);
+cudaError_t launch_attn_fp8_d128(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                                 const AttnParams&, int grid, cudaStream_t);
+int status_attn_bf16_d64(bool clear);
+int status_attn_bf16_d128(bool clear);
+int status_attn_fp8_d128(bool clear);
+
+// FP8 operand preparation: x bf16 [BH][N][128] -> e4m3 (row layout, or
+// transposed [BH][128][Npad]) plus per-128-row-block scales.
+cudaError_t launch_fp8_prep(const void* x, void* x8, float* scales, const signed char* signs,
+                            int BH, int H, int N, int transpose_out, cudaStream_t stream);
+
+}  // namespace gb300

@@ -1,0 +1,133 @@
+/* attn.h -- C ABI of the GB300 (sm_103a) exact attention forward library.
+ *
+ * The operation is exact scaled-dot-product attention,
+ *     O   = softmax(scale * Q K^T  [+ causal mask]) V,
+ *     lse = log sum_j exp(scale * q_i . k_j)       (natural log, per query row),
+ * computed in one fused pass that never writes the N x N score matrix: the
+ * online softmax of "Learn: The Memory Wall & FlashAttention", section 5.1
+ * (running max m, running denominator l, one final O~ / l), with the
+ * logsumexp L = m + log(l) of section 5.3.  Causal masking is top-left
+ * aligned: key j is visible from query i iff j <= i ("4.3 FlashAttention 2 &
+ * 3: Work Partitioning, Warp Specialization & FP8", "Edit 1 -- defer the
+ * rescaling").  A row that sees no key would get O = 0, lse = -inf (it cannot
+ * occur for the square shapes accepted here).
+ *
+ * Conventions shared by every entry point:
+ *   - All tensor pointers are caller-owned DEVICE memory on the current CUDA
+ *     device.  The library allocates, frees and retains nothing; it keeps no
+ *     pointer after the call returns.
+ *   - Layout is [B, H, N, d] row-major, d innermost, contiguous (the layout of
+ *     torch's scaled_dot_product_attention, not flash-attn's [B, N, H, d]).
+ *     Queries and keys have the same length N.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream).  Return values report argument errors and launch
+ *     errors only; faults during execution surface at the caller's next
+ *     synchronisation, and a pipeline wait that runs out of time is reported
+ *     by attn_device_status().
+ *   - Every bounded wait inside a kernel gives up after a time limit (1 s for
+ *     the plain entry points), records ATTN_ERR_TIMEOUT, frees its tensor
+ *     memory and returns; outputs are then unspecified.
+ */
+#ifndef GB300_ATTN_H
+#define GB300_ATTN_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+typedef struct CUstream_st* attn_stream_t; /* == cudaStream_t */
+
+enum attn_status {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = -1, /* null pointer, bad size, non-finite scale, bad enum */
+  ATTN_ERR_UNSUPPORTED = -2, /* head dim / dtype / device not supported */
+  ATTN_ERR_ALIGNMENT = -3,   /* a tensor base address is not 16-byte aligned */
+  ATTN_ERR_CUDA = -4,        /* a CUDA runtime / driver call failed (launch, encode) */
+  ATTN_ERR_TIMEOUT = -5      /* a pipeline wait inside a kernel ran out of time */
+};
+
+enum attn_dtype { ATTN_BF16 = 0 };
+
+/* Exact attention forward, bf16 operands, f32 accumulation.
+ *   q, k, v : bf16 [B, H, N, d], read only.
+ *   o       : bf16 [B, H, N, d], written (round to nearest even).
+ *   lse     : f32 [B, H, N] logsumexp of the scaled scores, written; may be NULL.
+ *   B, H, N : >= 1 (B * H < 2^31, N < 2^31).   d : 64 or 128.
+ *   scale   : finite multiplier of q.k (usually 1/sqrt(d)).
+ *   causal  : 0 or 1.   dtype : ATTN_BF16.
+ * Errors: ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED (d, dtype, a device other than sm_103),
+ * ATTN_ERR_ALIGNMENT (any of q, k, v, o not 16-byte aligned, lse not 4-byte aligned),
+ * ATTN_ERR_CUDA. */
+ATTN_API int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+             int d, float scale, int causal, int dtype, attn_stream_t stream);
+
+/* Preparation of FP8 E4M3 operands with per-block scales and, optionally,
+ * incoherent processing ("4.3 FlashAttention 2 & 3", section "Incoherent
+ * processing: rotate away the outliers"; "FlashAttention-3: How Warp
+ * Specialization, Asynchronous TMA Tiling, and FP8 Hardware Acceleration Scale
+ * Attention on Hopper GPUs", section 4, block-wise scaling).
+ *   x      : bf16 [B, H, N, d] input (Q, K or V), read only.
+ *   signs  : int8 [H, d] of +1/-1, or NULL.  If given, each row x of head h is
+ *            first rotated to x H_d diag(signs[h]) with H_d the orthonormal
+ *            Sylvester Hadamard matrix (fast Walsh-Hadamard transform in f32);
+ *            Q and K of one head must use the same signs.  V passes NULL.
+ *   x8     : E4M3 output.  transpose_out == 0: [B, H, N, d].
+ *            transpose_out == 1: [B, H, d, Npad] with Npad = 128 * ceil(N/128),
+ *            keys contiguous, padding keys zero (the V operand layout that
+ *            attn_fwd_fp8 reads).
+ *   block_scale : f32 [B, H, ceil(N/128)], written: per block of 128 rows,
+ *            s = amax / 448 over the (rotated) block, or 1 if the block is all
+ *            zero; codes are RNE-satfinite E4M3 of x / s (f32 division).
+ *   d : 128.
+ * Errors: as attn_fwd (ATTN_ERR_ALIGNMENT: x, x8 not 16-byte aligned). */
+ATTN_API int attn_fp8_prep(const void* x, void* x8, float* block_scale, const signed char* signs, int B,
+                  int H, int N, int d, int transpose_out, attn_stream_t stream);
+
+/* Exact attention forward with E4M3 operands (f32 accumulation, f32 softmax
+ * statistics, bf16 output).  Score tile j of query block i is
+ * q_scale[i] * k_scale[j] * (Q8_i K8_j^T) * scale.  P is quantised to E4M3
+ * with V's block scale folded in (p * 256 * v_scale[j] / max_j v_scale[j]).
+ *   q8, k8  : E4M3 [B, H, N, d] from attn_fp8_prep (same signs for both).
+ *   v8t     : E4M3 [B, H, d, Npad] from attn_fp8_prep with transpose_out = 1.
+ *   q_scale, k_scale, v_scale : f32 [B, H, ceil(N/128)] block scales.
+ *   o, lse, B, H, N, scale, causal : as attn_fwd.   d : 128.
+ * Errors: as attn_fwd. */
+ATTN_API int attn_fwd_fp8(const void* q8, const void* k8, const void* v8t, const float* q_scale,
+                 const float* k_scale, const float* v_scale, void* o, float* lse, int B, int H,
+                 int N, int d, float scale, int causal, attn_stream_t stream);
+
+/* attn_fwd with an explicit status word and wait limit, for tests of the
+ * failure path.  dev_status: device int, set to ATTN_ERR_TIMEOUT by a kernel
+ * whose wait ran out (the caller clears it first).  timeout_ns: wait limit.
+ * skip_loads: 0 for normal operation; n > 0 makes the load warp stop after n
+ * K/V tiles so that consumer waits run out (the kernel then returns with the
+ * status set, without faulting). */
+ATTN_API int attn_fwd_debug(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                   int N, int d, float scale, int causal, int* dev_status,
+                   unsigned long long timeout_ns, int skip_loads, attn_stream_t stream);
+
+/* Synchronises the current device, then returns (and, if clear != 0, resets)
+ * the status recorded by kernels launched through attn_fwd / attn_fwd_fp8:
+ * ATTN_OK or ATTN_ERR_TIMEOUT; ATTN_ERR_CUDA if the synchronisation failed. */
+ATTN_API int attn_device_status(int clear);
+
+/* Work units (query-tile pairs of 256 rows) the persistent scheduler runs for
+ * this shape, and the grid it would launch on a device with `num_sms` SMs.
+ * Host-only arithmetic; lets tests check the schedule without a GPU. */
+ATTN_API int attn_num_units(int B, int H, int N);
+ATTN_API int attn_grid_size(int B, int H, int N, int num_sms);
+
+/* Static description of a status code. */
+ATTN_API const char* attn_status_str(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GB300_ATTN_H */

@@ -1,0 +1,92 @@
+"""The C-ABI library without a GPU: it loads, exports every declared entry
+point, and its host-side logic (argument validation, schedule arithmetic,
+status strings) behaves as include/attn.h states.  No kernel is launched."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import exact_attention_forward_fwd_gb300 as ga
+from exact_attention_forward_fwd_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return ga.lib()
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "attn.h")).read()
+    return re.findall(r"ATTN_API\s+[\w\s\*]+?\b(attn_\w+)\s*\(", text)
+
+
+def test_exports_every_declared_symbol(L):
+    names = _declared()
+    assert len(names) >= 8
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_strings(L):
+    for code in (0, -1, -2, -3, -4, -5):
+        s = ga.status_str(code)
+        assert s and s != "unknown status"
+    assert ga.status_str(123) == "unknown status"
+
+
+def test_schedule_arithmetic(L):
+    assert ga.num_units(2, 16, 8192) == 2 * 16 * 32
+    assert ga.num_units(1, 2, 256) == 2
+    assert ga.num_units(1, 1, 257) == 2
+    assert ga.num_units(1, 1, 1) == 1
+    assert ga.grid_size(2, 16, 8192, 152) == 152
+    assert ga.grid_size(1, 2, 256, 152) == 2
+    assert ga.num_units(0, 1, 1) == 0
+
+
+A = ctypes.c_void_p(0x10000)       # 16-byte aligned dummy addresses: never dereferenced,
+M = ctypes.c_void_p(0x10002)       # validation fails before any CUDA call
+
+
+def _fwd(L, q=A, k=A, v=A, o=A, lse=None, B=1, H=1, N=128, d=128, scale=0.1, causal=0, dtype=0):
+    return L.attn_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, None)
+
+
+def test_validation_codes(L):
+    assert _fwd(L, q=None) == ga.ATTN_ERR_INVALID_ARG
+    assert _fwd(L, B=0) == ga.ATTN_ERR_INVALID_ARG
+    assert _fwd(L, N=-1) == ga.ATTN_ERR_INVALID_ARG
+    assert _fwd(L, scale=float("nan")) == ga.ATTN_ERR_INVALID_ARG
+    assert _fwd(L, scale=float("inf")) == ga.ATTN_ERR_INVALID_ARG
+    assert _fwd(L, causal=2) == ga.ATTN_ERR_INVALID_ARG
+    assert _fwd(L, d=96) == ga.ATTN_ERR_UNSUPPORTED
+    assert _fwd(L, dtype=1) == ga.ATTN_ERR_UNSUPPORTED
+    assert _fwd(L, k=M) == ga.ATTN_ERR_ALIGNMENT
+    assert _fwd(L, o=M) == ga.ATTN_ERR_ALIGNMENT
+    assert L.attn_fp8_prep(A, A, A, None, 1, 1, 128, 64, 0, None) == ga.ATTN_ERR_UNSUPPORTED
+    assert L.attn_fp8_prep(A, A, A, None, 1, 1, 128, 128, 2, None) == ga.ATTN_ERR_INVALID_ARG
+    assert L.attn_fp8_prep(M, A, A, None, 1, 1, 128, 128, 0, None) == ga.ATTN_ERR_ALIGNMENT
+    assert L.attn_fwd_fp8(A, A, A, A, A, None, A, None, 1, 1, 128, 128, 0.1, 0,
+                          None) == ga.ATTN_ERR_INVALID_ARG
+    assert L.attn_fwd_debug(A, A, A, A, None, 1, 1, 128, 128, 0.1, 0, None, 1000, 0,
+                            None) == ga.ATTN_ERR_INVALID_ARG
+
+
+def test_valid_args_without_gpu_report_no_device(L):
+    """All checks pass, so the device query runs: with no GPU it reports a
+    CUDA error (or 'unsupported' on a non-sm_103 device), never success."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert _fwd(L) in (ga.ATTN_ERR_CUDA, ga.ATTN_ERR_UNSUPPORTED)
+
+
+def test_product_path_has_no_cpu_fallback():
+    import torch
+    q = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        ga.attn_fwd(q, q, q)

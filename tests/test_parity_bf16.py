@@ -1,0 +1,115 @@
+"""GPU parity of the bf16 attention forward (C ABI through the binding)
+against the float64 three-pass oracle, element by element.
+
+Small shapes (all rows) span several 128-row tiles, ragged tails, N = 1 and
+both head dims; the 2048-token workloads are checked on every row; the
+8192- and 32768-token workloads, in the launch configuration the benchmark
+times, on sampled rows (row 0, the last row, both sides of every 128-row
+boundary, plus random rows)."""
+import numpy as np
+import pytest
+import torch
+
+import exact_attention_forward_fwd_gb300 as ga
+from exact_attention_forward_fwd_gb300 import inputs
+from oracle import attention as oa
+from parity_util import assert_bf16_parity, f64, metrics
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from exact_attention_forward_fwd_gb300 import build
+    build.build()
+    assert ga.device_status(clear=True) == 0
+
+
+def _run(q, k, v, causal, scale=None, rows=None):
+    d = q.shape[-1]
+    scale = d ** -0.5 if scale is None else scale
+    o, lse = ga.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=causal, scale=scale)
+    assert ga.device_status() == 0
+    O_ref, L_ref = oa.attention(f64(q), f64(k), f64(v), scale, causal, rows=rows)
+    o, lse = o.cpu(), lse.cpu()
+    if rows is not None:
+        o, lse = o[:, :, rows], lse[:, :, rows]
+    return metrics(o, lse, O_ref, L_ref)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [1, 7, 128, 129, 255, 256, 257, 300, 640, 1000])
+def test_small_shapes(N, d, causal):
+    q, k, v = inputs.make_qkv(2, 3, N, d, seed=N * 7 + d + int(causal))
+    assert_bf16_parity(_run(q, k, v, causal), f"N={N} d={d} causal={causal}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_more_units_than_sms(causal):
+    """B*H*pairs = 512 units: every CTA of the persistent grid runs several."""
+    q, k, v = inputs.make_qkv(16, 16, 300, 64, seed=77)
+    assert_bf16_parity(_run(q, k, v, causal), "16x16x300")
+
+
+@pytest.mark.parametrize("scale", [1.0, 0.01, 0.3])
+def test_other_scales(scale):
+    q, k, v = inputs.make_qkv(1, 2, 384, 128, seed=5)
+    assert_bf16_parity(_run(q, k, v, True, scale=scale), f"scale={scale}")
+
+
+@pytest.mark.parametrize("name", ["n256_d64", "n2048_d128", "n2048_d128_causal", "n2048_d128_k8",
+                                  "n2048_d128_k8_causal"])
+def test_workload_all_rows(name):
+    w = inputs.WORKLOADS[name]
+    q, k, v = inputs.workload_inputs(w)
+    m = _run(q, k, v, w.causal, w.scale)
+    print(name, m)
+    assert_bf16_parity(m, name)
+
+
+@pytest.mark.parametrize("name", ["n8192_d128", "n8192_d128_causal", "n32768_d64_causal"])
+def test_workload_sampled_rows(name):
+    w = inputs.WORKLOADS[name]
+    q, k, v = inputs.workload_inputs(w)
+    rows = inputs.sample_rows(w.N, 64, w.seed)
+    m = _run(q, k, v, w.causal, w.scale, rows=rows)
+    print(name, len(rows), "rows", m)
+    assert_bf16_parity(m, name)
+
+
+def test_deterministic_and_lse_optional():
+    q, k, v = (t.cuda() for t in inputs.make_qkv(2, 4, 1000, 128, seed=9))
+    o1, l1 = ga.attn_fwd(q, k, v, causal=True)
+    o2, l2 = ga.attn_fwd(q, k, v, causal=True)
+    o3, l3 = ga.attn_fwd(q, k, v, causal=True, return_lse=False)
+    torch.cuda.synchronize()
+    assert l3 is None
+    assert torch.equal(o1, o2) and torch.equal(l1, l2) and torch.equal(o1, o3)
+
+
+def test_side_stream_matches_default_stream():
+    q, k, v = (t.cuda() for t in inputs.make_qkv(1, 4, 700, 64, seed=11))
+    o1, l1 = ga.attn_fwd(q, k, v, causal=False)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        o2, l2 = ga.attn_fwd(q, k, v, causal=False)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_c_abi_errors_on_device():
+    import ctypes
+    q = torch.zeros(1, 1, 256, 128, dtype=torch.bfloat16, device="cuda")
+    o = torch.empty_like(q)
+    L = ga.lib()
+    p = lambda t, off=0: ctypes.c_void_p(t.data_ptr() + off)
+    assert L.attn_fwd(p(q), p(q), p(q), p(o), None, 1, 1, 256, 96, 0.1, 0, 0, None) == -2
+    assert L.attn_fwd(p(q, 2), p(q), p(q), p(o), None, 1, 1, 255, 128, 0.1, 0, 0, None) == -3
+    assert L.attn_fwd(p(q), p(q), p(q), p(o), None, 1, 1, 256, 128, 0.1, 0, 0, None) == 0
+    torch.cuda.synchronize()
+    with pytest.raises(ValueError):
+        ga.attn_fwd(q.float(), q, q)
+    with pytest.raises(ValueError):
+        ga.attn_fwd(q.transpose(2, 3), q, q)
