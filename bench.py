@@ -107,6 +107,33 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def kernel_source_hash() -> str:
+    """Hash of the attention kernel sources; an ncu summary records the hash of
+    the sources it was taken on, so stale counters are never reported."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "exact_attention_forward_fwd_gb300", "csrc")
+    for name in ("attn_kernel.cuh", "ptx.cuh"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _profiled_traffic(name):
+    """DRAM bytes per launch from profiles/<name>.md ('dram_bytes_per_launch:' and
+    'kernel_source_hash:' lines), or None if absent or taken on other sources."""
+    import re
+    path = os.path.join(ROOT, "profiles", name + ".md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    m_h = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
+    if not m_b or not m_h or m_h.group(1) != kernel_source_hash():
+        return None
+    return float(m_b.group(1))
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     if ws == 1:
@@ -322,13 +349,7 @@ def run_mine(args):
                "sample": f"the whole {w.name} workload, every row of every head (float64 "
                          f"three-pass oracle, {secs:.1f} s)"}
 
-    traffic = None
-    tpath = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tpath):
-        try:
-            traffic = json.load(open(tpath)).get(f"attn_bf16_d{w.d}_{'causal' if w.causal else 'noncausal'}")
-        except Exception:
-            traffic = None
+    traffic = _profiled_traffic(f"attn_fwd_bf16_d{w.d}_{w.name}")
     if rank == 0:
         clocks = clk.summary()
         line = {
