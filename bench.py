@@ -134,6 +134,22 @@ def _profiled_traffic(name):
     return float(m_b.group(1))
 
 
+def max_over_ranks(x: float, dist=None, device="cpu") -> float:
+    """The slowest rank's time: all-reduce MAX (NCCL on CUDA tensors, gloo on CPU)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_rank: float, ms_max: float, world_size: int) -> float:
+    """Replicas: every rank runs the same workload; the job's throughput is the
+    units of all ranks over the slowest rank's time."""
+    return flops_per_rank * world_size / (ms_max * 1e-3) / 1e12
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     if ws == 1:
@@ -229,12 +245,7 @@ def run_mine(args):
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    def max_over_ranks(x):
-        if dist is None:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    mor = lambda x: max_over_ranks(x, dist, dev)
 
     # ---------------------------------------------------------------- main
     qh, kh, vh = inputs.workload_inputs(w)
@@ -250,9 +261,9 @@ def run_mine(args):
     barrier()
     if ga.device_status() != 0:
         raise RuntimeError("kernel status word set during the benchmark")
-    ms = max_over_ranks(ms)
+    ms = mor(ms)
     tflops_launch = w.flops / (ms * 1e-3) / 1e12
-    value = tflops_launch * ws
+    value = whole_job_tflops(w.flops, ms, ws)
 
     # ---------------------------------------------------------------- e2e
     qp, kp, vp = (t.pin_memory() for t in (qh, kh, vh))
@@ -270,7 +281,7 @@ def run_mine(args):
     for _ in range(2):
         e2e_step()
     barrier()
-    ms_e2e = max_over_ranks(_time_loop(e2e_step, max(3, args.steps // 2), stream))
+    ms_e2e = mor(_time_loop(e2e_step, max(3, args.steps // 2), stream))
     barrier()
     h2d = 3 * q.numel() * q.element_size()
     d2h = o.numel() * o.element_size() + lse.numel() * 4
@@ -303,9 +314,9 @@ def run_mine(args):
         for _ in range(args.warmup):
             full8()
         barrier()
-        ms8 = max_over_ranks(_time_loop(attn8, args.steps, stream))
-        ms8p = max_over_ranks(_time_loop(full8, args.steps, stream))
-        msprep = max_over_ranks(_time_loop(prep8, args.steps, stream))
+        ms8 = mor(_time_loop(attn8, args.steps, stream))
+        ms8p = mor(_time_loop(full8, args.steps, stream))
+        msprep = mor(_time_loop(prep8, args.steps, stream))
         barrier()
         prep_bytes = 3 * fq.numel() * 2 + 3 * fq.numel() + 3 * sq.numel() * 4
         t8 = wf.flops / (ms8 * 1e-3) / 1e12
@@ -323,16 +334,21 @@ def run_mine(args):
     # ------------------------------------------------------- other workloads
     others = {}
     if not args.no_extra:
-        for name in ("n8192_d128_causal", "n32768_d64_causal", "n2048_d128", "n2048_d128_causal"):
+        for name in ("n8192_d128_causal", "n32768_d64_causal", "n2048_d128", "n2048_d128_causal",
+                     "n8192_d128_gqa4_window4096"):
             wo = inputs.WORKLOADS[name]
             a, b, c = (t.to(dev) for t in inputs.workload_inputs(wo))
             oo = torch.empty_like(a)
             lo = torch.empty(wo.B, wo.H, wo.N, dtype=torch.float32, device=dev)
-            fn = lambda: ga.attn_fwd(a, b, c, causal=wo.causal, scale=wo.scale, out=oo, lse=lo)
+            if wo.H_kv or wo.window:
+                fn = lambda: ga.attn_fwd_ex(a, b, c, causal=wo.causal, window=wo.window,
+                                            scale=wo.scale, out=oo, lse=lo)
+            else:
+                fn = lambda: ga.attn_fwd(a, b, c, causal=wo.causal, scale=wo.scale, out=oo, lse=lo)
             for _ in range(args.warmup):
                 fn()
             barrier()
-            mso = max_over_ranks(_time_loop(fn, args.steps, stream))
+            mso = mor(_time_loop(fn, args.steps, stream))
             others[name] = {"tflops": wo.flops / (mso * 1e-3) / 1e12 * ws, "ms": mso}
             del a, b, c, oo, lo
         barrier()

@@ -9,6 +9,7 @@ not an sm_103 GPU, calls raise.
 
 Functions mirror the C entry points:
   attn_fwd(q, k, v, causal=False, scale=None, out=None, lse=None)
+  attn_fwd_ex(q, k, v, causal=False, window=0, scale=None, ...)   (grouped KV heads, window)
   fp8_prep(x, signs=None, transpose=False, out=None, scales=None)
   attn_fwd_fp8(q8, k8, v8t, q_scale, k_scale, v_scale, causal=False, scale=None, ...)
   attn_fwd_fp8_from_bf16(q, k, v, signs, causal=False, scale=None)
@@ -50,6 +51,7 @@ def lib() -> ctypes.CDLL:
     L = ctypes.CDLL(LIB_PATH)
     vp, i, f, fp = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_void_p
     L.attn_fwd.argtypes = [vp, vp, vp, vp, fp, i, i, i, i, f, i, i, vp]
+    L.attn_fwd_ex.argtypes = [vp, vp, vp, vp, fp, i, i, i, i, i, f, i, i, i, vp]
     L.attn_fp8_prep.argtypes = [vp, vp, fp, vp, i, i, i, i, i, vp]
     L.attn_fwd_fp8.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, i, i, i, i, f, i, vp]
     L.attn_fwd_debug.argtypes = [vp, vp, vp, vp, fp, i, i, i, i, f, i, vp,
@@ -59,7 +61,7 @@ def lib() -> ctypes.CDLL:
     L.attn_grid_size.argtypes = [i, i, i, i]
     L.attn_status_str.argtypes = [i]
     L.attn_status_str.restype = ctypes.c_char_p
-    for name in ("attn_fwd", "attn_fp8_prep", "attn_fwd_fp8", "attn_fwd_debug",
+    for name in ("attn_fwd", "attn_fwd_ex", "attn_fp8_prep", "attn_fwd_fp8", "attn_fwd_debug",
                  "attn_device_status", "attn_num_units", "attn_grid_size"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
@@ -137,6 +139,36 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None
         rc = lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d,
                             float(scale), int(bool(causal)), ATTN_BF16, _stream(q))
     _check(rc, "attn_fwd")
+    return out, lse
+
+
+def attn_fwd_ex(q, k, v, causal: bool = False, window: int = 0, scale: float | None = None,
+                out=None, lse=None, return_lse: bool = True):
+    """attn_fwd with grouped-query heads (k, v: [B, H_kv, N, d], H_kv | H) and an
+    optional causal sliding window of `window` keys.  Returns (O, lse)."""
+    torch = _torch()
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, name, torch.bfloat16)
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q, k, v must be [B, H, N, d] / [B, H_kv, N, d]")
+    B, H, N, d = q.shape
+    H_kv = k.shape[1]
+    if tuple(k.shape) != (B, H_kv, N, d) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError(f"k and v must be [B, H_kv, N, d] = {(B, H_kv, N, d)}")
+    if k.device != q.device or v.device != q.device:
+        raise ValueError("q, k, v must be on one device")
+    scale = d ** -0.5 if scale is None else scale
+    out = torch.empty_like(q) if out is None else out
+    _need(out, "out", torch.bfloat16, q.shape)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, (B, H, N))
+    with torch.cuda.device(q.device):
+        rc = lib().attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, H_kv, N, d,
+                               float(scale), int(bool(causal)), int(window), ATTN_BF16,
+                               _stream(q))
+    _check(rc, "attn_fwd_ex")
     return out, lse
 
 

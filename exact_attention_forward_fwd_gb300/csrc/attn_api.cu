@@ -46,12 +46,17 @@ int check_shape(int B, int H, int N, float scale, int causal) {
   return ATTN_OK;
 }
 
-AttnParams base_params(void* o, float* lse, int BH, int N, float scale, int causal) {
+AttnParams base_params(void* o, float* lse, int B, int H, int H_kv, int N, float scale,
+                       int causal, int window) {
   AttnParams p{};
+  const int BH = B * H;
   p.o = o;
   p.lse = lse;
   p.N = N;
   p.BH = BH;
+  p.H = H;
+  p.group = H / H_kv;
+  p.window = window;
   p.nkb = (N + 127) / 128;
   p.npairs = (N + 255) / 256;
   p.num_units = BH * p.npairs;
@@ -62,11 +67,13 @@ AttnParams base_params(void* o, float* lse, int BH, int N, float scale, int caus
 }
 
 int run_bf16(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-             int N, int d, float scale, int causal, int dtype, int* status,
+             int H_kv, int N, int d, float scale, int causal, int window, int dtype, int* status,
              unsigned long long timeout_ns, int skip_loads, cudaStream_t stream) {
   if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
   int rc = check_shape(B, H, N, scale, causal);
   if (rc) return rc;
+  if (H_kv < 1 || H % H_kv != 0) return ATTN_ERR_INVALID_ARG;
+  if (window < 0 || (window > 0 && !causal)) return ATTN_ERR_INVALID_ARG;
   if (dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
   if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
@@ -74,14 +81,14 @@ int run_bf16(const void* q, const void* k, const void* v, void* o, float* lse, i
     return ATTN_ERR_ALIGNMENT;
   int sms = 0;
   if ((rc = device_check(&sms))) return rc;
-  const int BH = B * H;
+  const int BH = B * H, BHk = B * H_kv;
   CUtensorMap mq, mk, mv;
   const uint32_t box_inner = 64;   // 128-byte rows of the swizzle atom
   if (!encode_map_3d(&mq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, N, BH, box_inner, 128) ||
-      !encode_map_3d(&mk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, N, BH, box_inner, 128) ||
-      !encode_map_3d(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, N, BH, box_inner, 128))
+      !encode_map_3d(&mk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, N, BHk, box_inner, 128) ||
+      !encode_map_3d(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, N, BHk, box_inner, 128))
     return ATTN_ERR_CUDA;
-  AttnParams p = base_params(o, lse, BH, N, scale, causal);
+  AttnParams p = base_params(o, lse, B, H, H_kv, N, scale, causal, window);
   p.status = status;
   p.timeout_ns = timeout_ns;
   p.skip_load = skip_loads;
@@ -97,8 +104,15 @@ extern "C" {
 
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
              int d, float scale, int causal, int dtype, attn_stream_t stream) {
-  return run_bf16(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, nullptr, kDefaultTimeoutNs,
-                  0, reinterpret_cast<cudaStream_t>(stream));
+  return run_bf16(q, k, v, o, lse, B, H, H, N, d, scale, causal, 0, dtype, nullptr,
+                  kDefaultTimeoutNs, 0, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                int H_kv, int N, int d, float scale, int causal, int window, int dtype,
+                attn_stream_t stream) {
+  return run_bf16(q, k, v, o, lse, B, H, H_kv, N, d, scale, causal, window, dtype, nullptr,
+                  kDefaultTimeoutNs, 0, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int attn_fwd_debug(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
@@ -106,8 +120,8 @@ int attn_fwd_debug(const void* q, const void* k, const void* v, void* o, float* 
                    unsigned long long timeout_ns, int skip_loads, attn_stream_t stream) {
   if (!dev_status || !aligned(dev_status, 4) || timeout_ns == 0 || skip_loads < 0)
     return ATTN_ERR_INVALID_ARG;
-  return run_bf16(q, k, v, o, lse, B, H, N, d, scale, causal, ATTN_BF16, dev_status, timeout_ns,
-                  skip_loads, reinterpret_cast<cudaStream_t>(stream));
+  return run_bf16(q, k, v, o, lse, B, H, H, N, d, scale, causal, 0, ATTN_BF16, dev_status,
+                  timeout_ns, skip_loads, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int attn_fp8_prep(const void* x, void* x8, float* block_scale, const signed char* signs, int B,
@@ -146,7 +160,7 @@ int attn_fwd_fp8(const void* q8, const void* k8, const void* v8t, const float* q
       !encode_map_3d(&mk, k8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, d, N, BH, 128, 128) ||
       !encode_map_3d(&mv, v8t, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Npad, d, BH, 128, 128))
     return ATTN_ERR_CUDA;
-  AttnParams p = base_params(o, lse, BH, N, scale, causal);
+  AttnParams p = base_params(o, lse, B, H, H, N, scale, causal, 0);
   p.q_scale = q_scale;
   p.k_scale = k_scale;
   p.v_scale = v_scale;

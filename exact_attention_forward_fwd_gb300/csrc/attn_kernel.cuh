@@ -64,7 +64,10 @@ struct AttnParams {
   const float* v_scale;  // FP8 only: [BH][nkb]
   int* status;           // device status word, or null for the library's own word
   int N;                 // sequence length (queries == keys)
-  int BH;                // batch * heads
+  int BH;                // batch * query heads
+  int H;                 // query heads
+  int group;             // query heads per KV head (H / H_kv)
+  int window;            // > 0: causal sliding window of this many keys; 0: none
   int nkb;               // ceil(N / 128): key blocks (and 128-row query tiles)
   int npairs;            // ceil(N / 256): query-tile pairs per head
   int num_units;         // BH * npairs
@@ -138,24 +141,32 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, cons
 }
 
 struct Unit {
-  int bh, pair, nblocks;
+  int bh, bhk, pair, j0, nblocks;   // query head, KV head, pair, first key block, blocks
 };
 
 // Work unit u -> (head, query-tile pair, key blocks to visit).  Non-causal:
 // consecutive units walk the pairs of one head (K/V of a head stay hot in L2).
-// Causal: longest first -- all heads' last pair, then the one before, ...
+// Causal: longest first -- all heads' last pair, then the one before, ...; a
+// sliding window also skips the key blocks entirely before the window of the
+// pair's first row.  Query head h of batch b reads KV head h / group.
 __device__ __forceinline__ Unit unit_of(int u, const AttnParams& p) {
   Unit w;
   if (p.causal) {
     const int r = u / p.BH;
     w.bh = u - r * p.BH;
     w.pair = p.npairs - 1 - r;
-    w.nblocks = min(p.nkb, 2 * w.pair + 2);
+    const int j_hi = min(p.nkb - 1, 2 * w.pair + 1);
+    w.j0 = p.window > 0 ? max(0, w.pair * 256 - p.window + 1) / 128 : 0;
+    w.nblocks = j_hi - w.j0 + 1;
   } else {
     w.bh = u / p.npairs;
     w.pair = u - w.bh * p.npairs;
+    w.j0 = 0;
     w.nblocks = p.nkb;
   }
+  const int b = w.bh / p.H;
+  const int h = w.bh - b * p.H;
+  w.bhk = b * (p.H / p.group) + h / p.group;
   return w;
 }
 
@@ -227,7 +238,8 @@ __global__ void __launch_bounds__(320, 1)
             tma_load_3d_hint(sQ + t * C::kTileBytes + s * 16384, &tmQ, bar(ctl.q_full[t]),
                              s * (FP8 ? 128 : 64), row0, w.bh, pol_q);
         }
-        for (int j = 0; j < w.nblocks && ok; ++j) {
+        for (int jj = 0; jj < w.nblocks && ok; ++jj) {
+          const int j = w.j0 + jj;   // key block
           for (int kv = 0; kv < 2 && ok; ++kv, ++item) {
             if (p.skip_load > 0 && loads >= p.skip_load) break;   // test hook only
             const uint32_t slot = item % C::kStages;
@@ -239,14 +251,14 @@ __global__ void __launch_bounds__(320, 1)
             if (kv == 0) {
               for (int s = 0; s < C::kSlabs; ++s)
                 tma_load_3d_hint(dst + s * 16384, &tmK, bar(ctl.kv_full[slot]),
-                                 s * (FP8 ? 128 : 64), j * 128, w.bh, pol_kv);
+                                 s * (FP8 ? 128 : 64), j * 128, w.bhk, pol_kv);
             } else if (FP8) {
               // V^T [BH][D][Npad]: one 128-key x D tile
-              tma_load_3d_hint(dst, &tmV, bar(ctl.kv_full[slot]), j * 128, 0, w.bh, pol_kv);
+              tma_load_3d_hint(dst, &tmV, bar(ctl.kv_full[slot]), j * 128, 0, w.bhk, pol_kv);
             } else {
               for (int s = 0; s < C::kSlabs; ++s)
                 tma_load_3d_hint(dst + s * 16384, &tmV, bar(ctl.kv_full[slot]), s * 64, j * 128,
-                                 w.bh, pol_kv);
+                                 w.bhk, pol_kv);
             }
             ++loads;
           }
@@ -366,6 +378,7 @@ __global__ void __launch_bounds__(320, 1)
       const Unit w = unit_of(u, p);
       const int row = w.pair * 256 + t * 128 + r;
       const int lim_row = p.causal ? min(row, p.N - 1) : p.N - 1;   // last visible key
+      const int lo_row = p.window > 0 ? row - p.window + 1 : 0;      // first visible key
       float m_ref = NEG_INF, ell = 0.0f;   // reference max (base 2), sum of f32 p
       float ell_r = 0.0f;                   // sum of p as rounded into P (bf16 path)
       float q_s = 1.0f, v_smax = 1.0f;
@@ -373,12 +386,13 @@ __global__ void __launch_bounds__(320, 1)
         const int qb = w.pair * 2 + t;
         q_s = (qb < p.nkb) ? __ldg(p.q_scale + (size_t)w.bh * p.nkb + qb) : 1.0f;
         float mx = 0.0f;
-        for (int b = lane; b < p.nkb; b += 32) mx = fmaxf(mx, __ldg(p.v_scale + (size_t)w.bh * p.nkb + b));
+        for (int b = lane; b < p.nkb; b += 32) mx = fmaxf(mx, __ldg(p.v_scale + (size_t)w.bhk * p.nkb + b));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         v_smax = mx;
       }
-      for (int j = 0; j < w.nblocks; ++j) {
+      for (int jj = 0; jj < w.nblocks; ++jj) {
+        const int j = w.j0 + jj;   // key block
         ok = wait_bounded(bar(ctl.s_full[t]), sit++ & 1, wc);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
@@ -396,13 +410,14 @@ __global__ void __launch_bounds__(320, 1)
         float cj = p.scale_log2;
         float v_fold = 1.0f;
         if (FP8) {
-          cj *= q_s * __ldg(p.k_scale + (size_t)w.bh * p.nkb + j);
-          v_fold = 256.0f * __ldg(p.v_scale + (size_t)w.bh * p.nkb + j) / v_smax;
+          cj *= q_s * __ldg(p.k_scale + (size_t)w.bhk * p.nkb + j);
+          v_fold = 256.0f * __ldg(p.v_scale + (size_t)w.bhk * p.nkb + j) / v_smax;
         }
         const int lim = lim_row - j * 128;    // columns > lim are invisible
-        if (lim < 127) {
+        const int lo = lo_row - j * 128;      // columns < lo are invisible (window)
+        if (lim < 127 || lo > 0) {
 #pragma unroll
-          for (int c = 0; c < 128; ++c) x[c] = (c > lim) ? NEG_INF : x[c];
+          for (int c = 0; c < 128; ++c) x[c] = (c > lim || c < lo) ? NEG_INF : x[c];
         }
         float m0 = x[0], m1 = x[1], m2 = x[2], m3 = x[3];
 #pragma unroll
@@ -417,7 +432,7 @@ __global__ void __launch_bounds__(320, 1)
         const bool need = m_blk > m_ref + tau;
         const float m_new = need ? m_blk : m_ref;
         const float alpha = need ? ex2_approx(m_ref - m_new) : 1.0f;   // 0 when m_ref = -inf
-        if (j > 0 && __any_sync(0xffffffffu, need)) {
+        if (jj > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll 1
           for (int cc = 0; cc < D; cc += 32) {
             uint32_t orow[32];

@@ -39,6 +39,12 @@ class Workload:
     seed: int = 1000
     k_scale: float = 1.0
     outlier_frac: float = 0.0
+    H_kv: int = 0              # KV heads (0: same as H)
+    window: int = 0            # causal sliding window in keys (0: none)
+
+    @property
+    def kv_heads(self) -> int:
+        return self.H_kv or self.H
 
     @property
     def scale(self) -> float:
@@ -46,7 +52,12 @@ class Workload:
 
     @property
     def flops(self) -> float:
-        """4*B*H*N^2*d, halved for causal (the usual attention-forward convention)."""
+        """4*B*H*N^2*d, halved for causal (the usual attention-forward convention);
+        with a sliding window, 4*d per visible (query, key) pair."""
+        if self.window > 0:
+            n, w = self.N, min(self.window, self.N)
+            pairs = w * (w + 1) / 2 + (n - w) * w
+            return 4.0 * self.B * self.H * self.d * pairs
         f = 4.0 * self.B * self.H * self.N * self.N * self.d
         return f / 2 if self.causal else f
 
@@ -66,6 +77,10 @@ WORKLOADS = {
     "n32768_d64_causal": Workload("n32768_d64_causal", 1, 8, 32768, 64, True, seed=1004),
     "fp8_n8192_d128": Workload("fp8_n8192_d128", 2, 16, 8192, 128, False, dtype="fp8",
                                seed=1005, outlier_frac=0.001),
+    # Grouped-query heads (16 query heads share 4 KV heads) with a causal 4096-key
+    # sliding window, the shape of the FA2/3 page's flash_attn_func example.
+    "n8192_d128_gqa4_window4096": Workload("n8192_d128_gqa4_window4096", 2, 16, 8192, 128, True,
+                                           seed=1006, H_kv=4, window=4096),
 }
 
 
@@ -90,12 +105,13 @@ def _inject_outliers(x: torch.Tensor, frac: float, seed: int) -> torch.Tensor:
 
 
 def make_qkv(B: int, H: int, N: int, d: int, seed: int, k_scale: float = 1.0,
-             outlier_frac: float = 0.0):
-    """Return (q, k, v) as bfloat16 CPU tensors of shape [B, H, N, d]."""
-    shape = (B, H, N, d)
+             outlier_frac: float = 0.0, H_kv: int = 0):
+    """Return (q, k, v) as bfloat16 CPU tensors: q [B, H, N, d], k and v
+    [B, H_kv, N, d] (H_kv = H when 0)."""
+    shapes = [(B, H, N, d), (B, H_kv or H, N, d), (B, H_kv or H, N, d)]
     out = []
     for i in range(3):
-        x = torch.randn(shape, generator=_gen(seed * 16 + i), dtype=torch.float32)
+        x = torch.randn(shapes[i], generator=_gen(seed * 16 + i), dtype=torch.float32)
         if outlier_frac:
             x = _inject_outliers(x, outlier_frac, seed * 16 + 3 + i)
         out.append(x.to(torch.bfloat16))
@@ -114,7 +130,7 @@ def make_signs(H: int, d: int, seed: int) -> torch.Tensor:
 
 def workload_inputs(w: Workload):
     """(q, k, v) for a catalogue workload, bfloat16 CPU tensors."""
-    return make_qkv(w.B, w.H, w.N, w.d, w.seed, w.k_scale, w.outlier_frac)
+    return make_qkv(w.B, w.H, w.N, w.d, w.seed, w.k_scale, w.outlier_frac, w.H_kv)
 
 
 def sample_rows(N: int, count: int, seed: int, tile: int = 128):

@@ -67,6 +67,20 @@ enum attn_dtype { ATTN_BF16 = 0 };
 ATTN_API int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
              int d, float scale, int causal, int dtype, attn_stream_t stream);
 
+/* attn_fwd generalised to grouped-query heads and a causal sliding window
+ * ("4.3 FlashAttention 2 & 3", section "Calling the real kernel": KV heads
+ * divide the query heads, no KV replication; Exercise 5: query i attends to
+ * keys j with i - window < j <= i, blocks entirely outside the window skipped).
+ *   q, o    : bf16 [B, H, N, d];  k, v : bf16 [B, H_kv, N, d]; query head h of
+ *             batch b reads KV head h / (H / H_kv).  lse : f32 [B, H, N] or NULL.
+ *   H_kv    : >= 1, divides H (H_kv = H: multi-head; 1: multi-query).
+ *   window  : 0 for none; > 0 requires causal = 1.
+ * Other arguments and errors as attn_fwd (ATTN_ERR_INVALID_ARG for a bad H_kv
+ * or window). */
+ATTN_API int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                         int H, int H_kv, int N, int d, float scale, int causal, int window,
+                         int dtype, attn_stream_t stream);
+
 /* Preparation of FP8 E4M3 operands with per-block scales and, optionally,
  * incoherent processing ("4.3 FlashAttention 2 & 3", section "Incoherent
  * processing: rotate away the outliers"; "FlashAttention-3: How Warp

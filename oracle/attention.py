@@ -16,6 +16,10 @@ Sources (page titles, with the part of each page that is followed):
   * "FlashAttention-3 & GPU Kernel Optimization: Accelerating Transformer
     Attention", section "Online softmax tiling mathematics": the merge of two
     partial softmax states (m1, l1, O1) and (m2, l2, O2).
+  * "4.3 FlashAttention 2 & 3", section "Calling the real kernel": grouped-query
+    attention, where KV heads divide the query heads and query head h reads KV
+    head h // (H / H_kv); Exercise 5: a causal sliding window of width w, query
+    i sees keys j with i - w < j <= i.
 
 Conventions: q, k, v are float64 arrays [B, H, N, d]; ``scale`` multiplies the
 raw dot products; lse is the natural log of the sum of exp of the *scaled*
@@ -27,11 +31,12 @@ from __future__ import annotations
 import numpy as np
 
 
-def three_pass_rows(q, k, v, scale: float, causal: bool, rows):
+def three_pass_rows(q, k, v, scale: float, causal: bool, rows, window: int = 0):
     """Three-pass attention for the listed query rows of one (batch, head).
 
     q: [N, d], k: [N, d], v: [N, d] float64.  Returns (O [len(rows), d],
-    lse [len(rows)]).  The score row S_i is materialised in full.
+    lse [len(rows)]).  The score row S_i is materialised in full.  window > 0
+    (causal only) additionally hides keys j <= i - window.
     """
     rows = np.asarray(rows, dtype=np.int64)
     N = k.shape[0]
@@ -44,6 +49,8 @@ def three_pass_rows(q, k, v, scale: float, causal: bool, rows):
     if causal:
         keys = np.arange(N)[None, :]
         S = np.where(keys <= rows[:, None], S, -np.inf)
+        if window > 0:
+            S = np.where(keys > rows[:, None] - window, S, -np.inf)
     # Pass 1: row max over visible keys.
     m = S.max(axis=1)
     live = np.isfinite(m)
@@ -60,14 +67,21 @@ def three_pass_rows(q, k, v, scale: float, causal: bool, rows):
     return out, lse
 
 
-def attention(q, k, v, scale: float, causal: bool, rows=None, row_chunk: int = 512):
+def attention(q, k, v, scale: float, causal: bool, rows=None, row_chunk: int = 512,
+              window: int = 0):
     """Three-pass attention for every (batch, head).
 
-    If ``rows`` is given, only those query rows are computed (the same rows
-    for every (b, h)); outputs then have N replaced by len(rows).
+    q: [B, H, N, d]; k, v: [B, H_kv, N, d] with H_kv dividing H (query head h
+    reads KV head h // (H / H_kv)).  If ``rows`` is given, only those query rows
+    are computed (the same rows for every (b, h)); outputs then have N replaced
+    by len(rows).  window > 0 with causal: sliding window of that many keys.
     Returns (O, lse) as float64 arrays.
     """
     B, H, N, d = q.shape
+    H_kv = k.shape[1]
+    if H % H_kv:
+        raise ValueError("KV heads must divide query heads")
+    group = H // H_kv
     sel = np.arange(N) if rows is None else np.asarray(rows, dtype=np.int64)
     O = np.zeros((B, H, sel.size, v.shape[-1]), dtype=np.float64)
     L = np.zeros((B, H, sel.size), dtype=np.float64)
@@ -75,7 +89,8 @@ def attention(q, k, v, scale: float, causal: bool, rows=None, row_chunk: int = 5
         for h in range(H):
             for c0 in range(0, sel.size, row_chunk):
                 r = sel[c0:c0 + row_chunk]
-                o, l = three_pass_rows(q[b, h], k[b, h], v[b, h], scale, causal, r)
+                o, l = three_pass_rows(q[b, h], k[b, h // group], v[b, h // group], scale,
+                                       causal, r, window)
                 O[b, h, c0:c0 + r.size] = o
                 L[b, h, c0:c0 + r.size] = l
     return O, L

@@ -6,7 +6,10 @@ import torch
 # |O - O_ref| <= 1e-2 + 2^-9 |O_ref|: the 1e-2 bound on top of the half-unit
 # rounding of the bf16 output format itself (a bf16 O in [4, 8) cannot be
 # nearer than 2^-6 to a value between two representable numbers; on the K*8
-# workload the exactly rounded oracle result is already 0.015 away).
+# workload the exactly rounded oracle result is already 0.015 away).  The mean
+# abs bound gets the same allowance on average, 1e-3 + 2^-9 mean|O_ref|: for
+# rows that see one or two keys (short windows) O is of unit size and rounding
+# it to bf16 alone averages about 1e-3; for long rows the term is ~4e-5.
 BF16_MAX_ABS = 1e-2
 BF16_OUT_HALF_ULP = 2.0 ** -9
 BF16_MEAN_ABS = 1e-3
@@ -35,6 +38,7 @@ def metrics(o_gpu, lse_gpu, O_ref, L_ref):
         "max_abs": float(err.max()),
         "max_excess": float((err - BF16_OUT_HALF_ULP * np.abs(O_ref)).max()),
         "mean_abs": float(err.mean()),
+        "mean_half_ulp": float(BF16_OUT_HALF_ULP * np.abs(O_ref).mean()),
         "rmse": float(np.sqrt((err ** 2).mean())),
         "rel_rmse": float(np.sqrt((err ** 2).mean() / max((O_ref ** 2).mean(), 1e-300))),
         "lse_max_abs": float(lerr.max()),
@@ -46,7 +50,8 @@ def assert_bf16_parity(m, what=""):
     assert m["finite"], f"{what}: non-finite output"
     assert m["max_excess"] <= BF16_MAX_ABS, \
         f"{what}: max abs {m['max_abs']:.3e} (beyond output rounding {m['max_excess']:.3e})"
-    assert m["mean_abs"] <= BF16_MEAN_ABS, f"{what}: mean abs {m['mean_abs']:.3e}"
+    assert m["mean_abs"] <= BF16_MEAN_ABS + m["mean_half_ulp"], \
+        f"{what}: mean abs {m['mean_abs']:.3e} (output rounding allowance {m['mean_half_ulp']:.1e})"
     assert m["lse_max_abs"] <= LSE_MAX_ABS, f"{what}: lse max abs {m['lse_max_abs']:.3e}"
 
 

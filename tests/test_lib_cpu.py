@@ -76,6 +76,25 @@ def test_validation_codes(L):
                             None) == ga.ATTN_ERR_INVALID_ARG
 
 
+def test_ex_validation_codes(L):
+    ex = lambda H=4, H_kv=2, causal=1, window=0, d=128: L.attn_fwd_ex(
+        A, A, A, A, None, 1, H, H_kv, 256, d, 0.1, causal, window, 0, None)
+    assert ex(H_kv=3) == ga.ATTN_ERR_INVALID_ARG      # does not divide H
+    assert ex(H_kv=0) == ga.ATTN_ERR_INVALID_ARG
+    assert ex(window=-1) == ga.ATTN_ERR_INVALID_ARG
+    assert ex(causal=0, window=64) == ga.ATTN_ERR_INVALID_ARG   # windows are causal
+    assert ex(d=96) == ga.ATTN_ERR_UNSUPPORTED
+
+
+def test_window_flops_convention():
+    from exact_attention_forward_fwd_gb300 import inputs
+    w = inputs.WORKLOADS["n8192_d128_gqa4_window4096"]
+    pairs = sum(min(i + 1, 4096) for i in range(8192))
+    assert w.flops == 4.0 * 2 * 16 * 128 * pairs
+    q, k, v = inputs.make_qkv(1, 4, 16, 64, seed=1, H_kv=2)
+    assert q.shape == (1, 4, 16, 64) and k.shape == v.shape == (1, 2, 16, 64)
+
+
 def test_valid_args_without_gpu_report_no_device(L):
     """All checks pass, so the device query runs: with no GPU it reports a
     CUDA error (or 'unsupported' on a non-sm_103 device), never success."""

@@ -203,3 +203,44 @@ def test_row_subset_equals_full():
     Os, Ls = oa.attention(q, k, v, 0.3, True, rows=rows)
     np.testing.assert_array_equal(Os, O[:, :, rows])
     np.testing.assert_array_equal(Ls, L[:, :, rows])
+
+
+# ----------------------------------------------- grouped-query heads, window
+
+def test_gqa_equals_mha_with_repeated_kv_heads():
+    B, H, H_kv, N, d = 2, 6, 2, 40, 8
+    q = _rand((B, H, N, d), 100)
+    k, v = _rand((B, H_kv, N, d), 101), _rand((B, H_kv, N, d), 102)
+    for causal in (False, True):
+        O, L = oa.attention(q, k, v, 0.4, causal)
+        kr, vr = np.repeat(k, H // H_kv, axis=1), np.repeat(v, H // H_kv, axis=1)
+        O2, L2 = oa.attention(q, kr, vr, 0.4, causal)
+        np.testing.assert_array_equal(O, O2)
+        np.testing.assert_array_equal(L, L2)
+    with pytest.raises(ValueError):
+        oa.attention(q, _rand((B, 4, N, d), 1), _rand((B, 4, N, d), 2), 0.4, False)
+
+
+def test_window_special_cases():
+    N, d = 50, 8
+    q, k, v = (_rand((1, 1, N, d), 110 + i) for i in range(3))
+    Oc, Lc = oa.attention(q, k, v, 0.3, True)
+    Ow, Lw = oa.attention(q, k, v, 0.3, True, window=N)
+    np.testing.assert_array_equal(Ow, Oc)
+    np.testing.assert_array_equal(Lw, Lc)
+    O1, L1 = oa.attention(q, k, v, 0.3, True, window=1)       # only the diagonal key
+    np.testing.assert_array_equal(O1[0, 0], v[0, 0])
+    np.testing.assert_allclose(L1[0, 0], 0.3 * np.einsum("nd,nd->n", q[0, 0], k[0, 0]), rtol=1e-14)
+
+
+def test_window_row_equals_non_causal_on_its_key_slice():
+    """Row i with window w sees exactly keys max(0, i-w+1)..i: the non-causal
+    oracle on that slice must give the same row."""
+    N, d, w = 70, 8, 13
+    q, k, v = (_rand((N, d), 120 + i) for i in range(3))
+    Ow, Lw = oa.three_pass_rows(q, k, v, 0.5, True, np.arange(N), window=w)
+    for i in range(N):
+        lo = max(0, i - w + 1)
+        O1, L1 = oa.three_pass_rows(q[i:i + 1], k[lo:i + 1], v[lo:i + 1], 0.5, False, [0])
+        np.testing.assert_allclose(Ow[i], O1[0], rtol=1e-12, atol=1e-14)
+        assert abs(Lw[i] - L1[0]) <= 1e-12 * max(1.0, abs(L1[0]))

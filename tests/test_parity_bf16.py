@@ -113,3 +113,53 @@ def test_c_abi_errors_on_device():
         ga.attn_fwd(q.float(), q, q)
     with pytest.raises(ValueError):
         ga.attn_fwd(q.transpose(2, 3), q, q)
+
+
+# -------------------------------------------------- grouped-query heads and windows
+
+def _run_ex(q, k, v, causal, window, rows=None):
+    d = q.shape[-1]
+    o, lse = ga.attn_fwd_ex(q.cuda(), k.cuda(), v.cuda(), causal=causal, window=window)
+    assert ga.device_status() == 0
+    O_ref, L_ref = oa.attention(f64(q), f64(k), f64(v), d ** -0.5, causal, rows=rows,
+                                window=window)
+    o, lse = o.cpu(), lse.cpu()
+    if rows is not None:
+        o, lse = o[:, :, rows], lse[:, :, rows]
+    return metrics(o, lse, O_ref, L_ref)
+
+
+@pytest.mark.parametrize("H_kv", [1, 2, 8])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_grouped_query_heads(H_kv, d, causal):
+    q, k, v = inputs.make_qkv(2, 8, 700, d, seed=300 + H_kv + d, H_kv=H_kv)
+    assert_bf16_parity(_run_ex(q, k, v, causal, 0), f"H_kv={H_kv} d={d}")
+
+
+@pytest.mark.parametrize("window", [1, 2, 64, 127, 128, 129, 255, 256, 300, 5000])
+def test_sliding_window(window):
+    q, k, v = inputs.make_qkv(1, 4, 1000, 128, seed=400 + window, H_kv=2)
+    assert_bf16_parity(_run_ex(q, k, v, True, window), f"window={window}")
+
+
+def test_sliding_window_d64_ragged():
+    q, k, v = inputs.make_qkv(3, 2, 777, 64, seed=501)
+    assert_bf16_parity(_run_ex(q, k, v, True, 200), "window=200 d=64")
+
+
+def test_gqa_window_workload_sampled_rows():
+    w = inputs.WORKLOADS["n8192_d128_gqa4_window4096"]
+    q, k, v = inputs.workload_inputs(w)
+    rows = inputs.sample_rows(w.N, 64, w.seed)
+    m = _run_ex(q, k, v, True, w.window, rows=rows)
+    print(w.name, len(rows), "rows", m)
+    assert_bf16_parity(m, w.name)
+
+
+def test_window_of_n_equals_plain_causal():
+    q, k, v = (t.cuda() for t in inputs.make_qkv(1, 2, 600, 128, seed=502))
+    o1, l1 = ga.attn_fwd(q, k, v, causal=True)
+    o2, l2 = ga.attn_fwd_ex(q, k, v, causal=True, window=600)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
