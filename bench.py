@@ -172,6 +172,23 @@ def _time_loop(fn, steps, stream):
     return e0.elapsed_time(e1) / steps   # ms per step
 
 
+def _time_loop_flushed(fn, steps, stream, flush):
+    """Mean ms of fn over `steps` launches, each timed alone after a write of
+    `flush` (larger than L2) so that no launch finds its inputs in L2."""
+    import torch
+    total = 0.0
+    for _ in range(steps):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        e1.synchronize()
+        total += e0.elapsed_time(e1)
+    return total / steps
+
+
 def _oracle_run(q, k, v, w, heads, threads):
     """Time the float64 oracle on every query row of the listed (b, h) slices of
     the workload's own inputs (CPU bf16 tensors); returns (seconds, flops)."""
@@ -334,8 +351,12 @@ def run_mine(args):
     # ------------------------------------------------------- other workloads
     others = {}
     if not args.no_extra:
+        # Each launch is timed alone after a 256 MiB write that flushes L2 (some
+        # of these workloads fit in L2).
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
         for name in ("n8192_d128_causal", "n32768_d64_causal", "n2048_d128", "n2048_d128_causal",
-                     "n8192_d128_gqa4_window4096"):
+                     "n8192_d128_gqa4_window4096", "n8192_d128_b1h2", "n8192_d128_b1h2_causal"):
             wo = inputs.WORKLOADS[name]
             a, b, c = (t.to(dev) for t in inputs.workload_inputs(wo))
             oo = torch.empty_like(a)
@@ -348,9 +369,25 @@ def run_mine(args):
             for _ in range(args.warmup):
                 fn()
             barrier()
-            mso = mor(_time_loop(fn, args.steps, stream))
-            others[name] = {"tflops": wo.flops / (mso * 1e-3) / 1e12 * ws, "ms": mso}
+            mso = mor(_time_loop_flushed(fn, args.steps, stream, flush))
+            others[name] = {"tflops": wo.flops / (mso * 1e-3) / 1e12 * ws, "ms": mso,
+                            "l2": "flushed before each launch"}
+            if name.startswith("n8192_d128_b1h2"):
+                # Split-KV on the same inputs, with the split count that fills the SMs.
+                S = ga.splitkv_default_splits(wo.B, wo.H, wo.N, sms)
+                wsp = torch.empty(ga.splitkv_workspace_bytes(wo.B, wo.H, wo.N, wo.d, S),
+                                  dtype=torch.uint8, device=dev)
+                fs = lambda: ga.attn_fwd_splitkv(a, b, c, causal=wo.causal, scale=wo.scale,
+                                                 num_splits=S, workspace=wsp, out=oo, lse=lo)
+                for _ in range(args.warmup):
+                    fs()
+                barrier()
+                mss = mor(_time_loop_flushed(fs, args.steps, stream, flush))
+                others[name]["splitkv"] = {"tflops": wo.flops / (mss * 1e-3) / 1e12 * ws,
+                                           "ms": mss, "splits": S, "launches_per_call": 2}
+                del wsp
             del a, b, c, oo, lo
+        del flush
         barrier()
     if ga.device_status() != 0:
         raise RuntimeError("kernel status word set during the benchmark")

@@ -10,6 +10,8 @@ not an sm_103 GPU, calls raise.
 Functions mirror the C entry points:
   attn_fwd(q, k, v, causal=False, scale=None, out=None, lse=None)
   attn_fwd_ex(q, k, v, causal=False, window=0, scale=None, ...)   (grouped KV heads, window)
+  attn_fwd_splitkv(q, k, v, causal=False, window=0, num_splits=None, workspace=None, ...)
+  splitkv_workspace_bytes(B, H, N, d, num_splits), splitkv_default_splits(B, H, N, num_sms)
   fp8_prep(x, signs=None, transpose=False, out=None, scales=None)
   attn_fwd_fp8(q8, k8, v8t, q_scale, k_scale, v_scale, causal=False, scale=None, ...)
   attn_fwd_fp8_from_bf16(q, k, v, signs, causal=False, scale=None)
@@ -59,10 +61,16 @@ def lib() -> ctypes.CDLL:
     L.attn_device_status.argtypes = [i]
     L.attn_num_units.argtypes = [i, i, i]
     L.attn_grid_size.argtypes = [i, i, i, i]
+    L.attn_fwd_splitkv.argtypes = [vp, vp, vp, vp, fp, i, i, i, i, i, f, i, i, i, i, vp,
+                                   ctypes.c_size_t, vp]
+    L.attn_splitkv_workspace_bytes.argtypes = [i, i, i, i, i]
+    L.attn_splitkv_workspace_bytes.restype = ctypes.c_size_t
+    L.attn_splitkv_default_splits.argtypes = [i, i, i, i]
     L.attn_status_str.argtypes = [i]
     L.attn_status_str.restype = ctypes.c_char_p
     for name in ("attn_fwd", "attn_fwd_ex", "attn_fp8_prep", "attn_fwd_fp8", "attn_fwd_debug",
-                 "attn_device_status", "attn_num_units", "attn_grid_size"):
+                 "attn_device_status", "attn_num_units", "attn_grid_size", "attn_fwd_splitkv",
+                 "attn_splitkv_default_splits"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -169,6 +177,57 @@ def attn_fwd_ex(q, k, v, causal: bool = False, window: int = 0, scale: float | N
                                float(scale), int(bool(causal)), int(window), ATTN_BF16,
                                _stream(q))
     _check(rc, "attn_fwd_ex")
+    return out, lse
+
+
+def splitkv_workspace_bytes(B: int, H: int, N: int, d: int, num_splits: int) -> int:
+    """Bytes of device workspace attn_fwd_splitkv needs (0 for invalid arguments)."""
+    return int(lib().attn_splitkv_workspace_bytes(B, H, N, d, num_splits))
+
+
+def splitkv_default_splits(B: int, H: int, N: int, num_sms: int) -> int:
+    """Split count that fills num_sms SMs for this shape (0 for invalid arguments)."""
+    return int(lib().attn_splitkv_default_splits(B, H, N, num_sms))
+
+
+def attn_fwd_splitkv(q, k, v, causal: bool = False, window: int = 0, scale: float | None = None,
+                     num_splits: int | None = None, workspace=None, out=None, lse=None,
+                     return_lse: bool = True):
+    """Split-KV attention forward (k, v may have fewer heads, as attn_fwd_ex).
+    num_splits defaults to the count that fills the device; workspace (a CUDA
+    uint8 tensor of at least splitkv_workspace_bytes(...) bytes) is allocated
+    here when not given.  Returns (O, lse)."""
+    torch = _torch()
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, name, torch.bfloat16)
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q, k, v must be [B, H, N, d] / [B, H_kv, N, d]")
+    B, H, N, d = q.shape
+    H_kv = k.shape[1]
+    if tuple(k.shape) != (B, H_kv, N, d) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError(f"k and v must be [B, H_kv, N, d] = {(B, H_kv, N, d)}")
+    if k.device != q.device or v.device != q.device:
+        raise ValueError("q, k, v must be on one device")
+    scale = d ** -0.5 if scale is None else scale
+    if num_splits is None:
+        sms = torch.cuda.get_device_properties(q.device).multi_processor_count
+        num_splits = splitkv_default_splits(B, H, N, sms)
+    need = splitkv_workspace_bytes(B, H, N, d, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    _need(workspace, "workspace", torch.uint8)
+    out = torch.empty_like(q) if out is None else out
+    _need(out, "out", torch.bfloat16, q.shape)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, (B, H, N))
+    with torch.cuda.device(q.device):
+        rc = lib().attn_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, H_kv,
+                                    N, d, float(scale), int(bool(causal)), int(window), ATTN_BF16,
+                                    int(num_splits), _ptr(workspace), workspace.numel(),
+                                    _stream(q))
+    _check(rc, "attn_fwd_splitkv")
     return out, lse
 
 

@@ -63,12 +63,33 @@ AttnParams base_params(void* o, float* lse, int B, int H, int H_kv, int N, float
   p.causal = causal;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.timeout_ns = kDefaultTimeoutNs;
+  p.splits = 1;
   return p;
 }
 
+constexpr int kMaxSplits = 64;
+
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+// Bytes of the split-KV workspace: partial O, then partial lse (each 256-aligned).
+size_t splitkv_bytes(int B, int H, int N, int d, int splits, size_t* lse_offset) {
+  const size_t rows = static_cast<size_t>(splits) * static_cast<size_t>(B) * H * N;
+  const size_t o_bytes = round256(rows * d * sizeof(float));
+  if (lse_offset) *lse_offset = o_bytes;
+  return o_bytes + round256(rows * sizeof(float));
+}
+
+// Split-KV arguments of run_bf16 (splits == 0: the plain path).
+struct SplitArgs {
+  int splits = 0;
+  void* workspace = nullptr;
+  size_t workspace_bytes = 0;
+};
+
 int run_bf16(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
              int H_kv, int N, int d, float scale, int causal, int window, int dtype, int* status,
-             unsigned long long timeout_ns, int skip_loads, cudaStream_t stream) {
+             unsigned long long timeout_ns, int skip_loads, cudaStream_t stream,
+             const SplitArgs& split = SplitArgs()) {
   if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
   int rc = check_shape(B, H, N, scale, causal);
   if (rc) return rc;
@@ -76,8 +97,16 @@ int run_bf16(const void* q, const void* k, const void* v, void* o, float* lse, i
   if (window < 0 || (window > 0 && !causal)) return ATTN_ERR_INVALID_ARG;
   if (dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
   if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  size_t lse_off = 0;
+  if (split.splits != 0) {
+    if (split.splits < 1 || split.splits > kMaxSplits || !split.workspace) return ATTN_ERR_INVALID_ARG;
+    if (static_cast<long long>(B) * H * ((N + 255) / 256) * split.splits > 0x7fffffffLL)
+      return ATTN_ERR_INVALID_ARG;
+    if (split.workspace_bytes < splitkv_bytes(B, H, N, d, split.splits, &lse_off))
+      return ATTN_ERR_INVALID_ARG;
+  }
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
-      (lse && !aligned(lse, 4)))
+      (lse && !aligned(lse, 4)) || (split.workspace && !aligned(split.workspace, 16)))
     return ATTN_ERR_ALIGNMENT;
   int sms = 0;
   if ((rc = device_check(&sms))) return rc;
@@ -92,9 +121,17 @@ int run_bf16(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.status = status;
   p.timeout_ns = timeout_ns;
   p.skip_load = skip_loads;
+  if (split.splits != 0) {
+    p.splits = split.splits;
+    p.num_units *= split.splits;
+    p.o_part = static_cast<float*>(split.workspace);
+    p.lse_part = reinterpret_cast<float*>(static_cast<char*>(split.workspace) + lse_off);
+  }
   const int grid = p.num_units < sms ? p.num_units : sms;
   cudaError_t e = (d == 64) ? launch_attn_bf16_d64(mq, mk, mv, p, grid, stream)
                             : launch_attn_bf16_d128(mq, mk, mv, p, grid, stream);
+  if (e == cudaSuccess && split.splits != 0)
+    e = launch_splitkv_merge(p.o_part, p.lse_part, o, lse, split.splits, BH, N, d, stream);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -113,6 +150,45 @@ int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse
                 attn_stream_t stream) {
   return run_bf16(q, k, v, o, lse, B, H, H_kv, N, d, scale, causal, window, dtype, nullptr,
                   kDefaultTimeoutNs, 0, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int H, int H_kv, int N, int d, float scale, int causal, int window, int dtype,
+                     int num_splits, void* workspace, size_t workspace_bytes,
+                     attn_stream_t stream) {
+  if (num_splits < 1 || num_splits > kMaxSplits) return ATTN_ERR_INVALID_ARG;
+  SplitArgs split;
+  split.splits = num_splits;
+  split.workspace = workspace;
+  split.workspace_bytes = workspace_bytes;
+  return run_bf16(q, k, v, o, lse, B, H, H_kv, N, d, scale, causal, window, dtype, nullptr,
+                  kDefaultTimeoutNs, 0, reinterpret_cast<cudaStream_t>(stream), split);
+}
+
+size_t attn_splitkv_workspace_bytes(int B, int H, int N, int d, int num_splits) {
+  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return 0;
+  if (num_splits < 1 || num_splits > kMaxSplits) return 0;
+  return splitkv_bytes(B, H, N, d, num_splits, nullptr);
+}
+
+int attn_splitkv_default_splits(int B, int H, int N, int num_sms) {
+  if (B < 1 || H < 1 || N < 1 || num_sms < 1) return 0;
+  const long long units = static_cast<long long>(B) * H * ((N + 255) / 256);
+  if (units >= num_sms) return 1;
+  // Fraction of the SM slots of whole waves that the units of S splits fill.
+  auto fill = [&](long long S) {
+    const long long u = units * S;
+    const long long waves = (u + num_sms - 1) / num_sms;
+    return static_cast<double>(u) / static_cast<double>(waves * num_sms);
+  };
+  const long long blocks = (N + 127) / 128;
+  const long long cap = blocks < kMaxSplits ? blocks : kMaxSplits;
+  long long best = 1;
+  for (long long S = 1; S <= cap; ++S) {
+    if (fill(S) >= 0.9) return static_cast<int>(S);
+    if (fill(S) > fill(best)) best = S;
+  }
+  return static_cast<int>(best);
 }
 
 int attn_fwd_debug(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,

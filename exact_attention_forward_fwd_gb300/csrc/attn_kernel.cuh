@@ -75,6 +75,13 @@ struct AttnParams {
   float scale_log2;      // scale * log2(e)
   unsigned long long timeout_ns;
   int skip_load;         // test hook: when > 0, the load warp stops after that many K/V loads
+  // Split-KV mode (o_part != null): every (head, query-tile pair) is split into
+  // `splits` contiguous key ranges, each a unit of its own, and each unit writes
+  // its partial result: O normalised by its own denominator, and its own
+  // logsumexp.  A merge kernel combines them.
+  int splits;            // key ranges per (head, pair); 1 without split-KV
+  float* o_part;         // [splits][BH][N][D] fp32, or null
+  float* lse_part;       // [splits][BH][N] fp32 (natural log), or null
 };
 
 template <int D, bool FP8>
@@ -115,7 +122,7 @@ struct SmemCtl {
 static __device__ int g_attn_status;
 
 struct WaitCtx {
-  SmemCtl* ctl;
+  int* abort_flag;   // this CTA's abort flag (shared memory)
   int* status;
   unsigned long long timeout_ns;
 };
@@ -124,16 +131,15 @@ struct WaitCtx {
 // abort or the limit ran out (which sets the abort flag and the status word).
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const WaitCtx& wc,
                                              bool honour_abort = true) {
-  SmemCtl* ctl = wc.ctl;
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (honour_abort && *reinterpret_cast<volatile int*>(&ctl->abort_flag)) return false;
+    if (honour_abort && *reinterpret_cast<volatile int*>(wc.abort_flag)) return false;
     if (global_timer_ns() - t0 > wc.timeout_ns) {
-      *reinterpret_cast<volatile int*>(&ctl->abort_flag) = 1;
+      *reinterpret_cast<volatile int*>(wc.abort_flag) = 1;
       atomicCAS(wc.status, kStatusOk, kStatusTimeout);
       return false;
     }
@@ -142,15 +148,25 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, cons
 
 struct Unit {
   int bh, bhk, pair, j0, nblocks;   // query head, KV head, pair, first key block, blocks
+  int split;                        // key range index (split-KV), 0 otherwise
 };
 
 // Work unit u -> (head, query-tile pair, key blocks to visit).  Non-causal:
 // consecutive units walk the pairs of one head (K/V of a head stay hot in L2).
 // Causal: longest first -- all heads' last pair, then the one before, ...; a
 // sliding window also skips the key blocks entirely before the window of the
-// pair's first row.  Query head h of batch b reads KV head h / group.
+// pair's first row.  Query head h of batch b reads KV head h / group.  With
+// split-KV, consecutive units are the key ranges of one pair: range s takes
+// blocks [s*nb/S, (s+1)*nb/S) of the pair's nb visible blocks (empty when
+// nb < S; such a unit only writes an empty partial result).
 __device__ __forceinline__ Unit unit_of(int u, const AttnParams& p) {
   Unit w;
+  const int S = p.splits > 1 ? p.splits : 1;
+  w.split = 0;
+  if (S > 1) {
+    w.split = u % S;
+    u /= S;
+  }
   if (p.causal) {
     const int r = u / p.BH;
     w.bh = u - r * p.BH;
@@ -163,6 +179,12 @@ __device__ __forceinline__ Unit unit_of(int u, const AttnParams& p) {
     w.pair = u - w.bh * p.npairs;
     w.j0 = 0;
     w.nblocks = p.nkb;
+  }
+  if (S > 1) {
+    const int nb = w.nblocks;
+    const int b0 = (w.split * nb) / S, b1 = ((w.split + 1) * nb) / S;
+    w.j0 += b0;
+    w.nblocks = b1 - b0;
   }
   const int b = w.bh / p.H;
   const int h = w.bh - b * p.H;
@@ -211,7 +233,7 @@ __global__ void __launch_bounds__(320, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl.tmem_base;
-  const WaitCtx wc{&ctl, p.status ? p.status : &g_attn_status, p.timeout_ns};
+  const WaitCtx wc{&ctl.abort_flag, p.status ? p.status : &g_attn_status, p.timeout_ns};
 
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
@@ -226,8 +248,9 @@ __global__ void __launch_bounds__(320, 1)
       uint32_t qn[2] = {0, 0};  // Q tiles issued per tile slot
       bool ok = true;
       int loads = 0;
-      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uit) {
+      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
         const Unit w = unit_of(u, p);
+        if (w.nblocks == 0) continue;   // empty key range (split-KV)
         for (int t = 0; t < 2 && ok; ++t) {
           if (uit > 0) ok = wait_bounded(bar(ctl.q_empty[t]), (uit - 1) & 1, wc);
           if (!ok) break;
@@ -263,6 +286,7 @@ __global__ void __launch_bounds__(320, 1)
             ++loads;
           }
         }
+        ++uit;
       }
       // Let every copy this warp started land before the CTA can exit.
       const uint32_t issued = item;
@@ -309,9 +333,10 @@ __global__ void __launch_bounds__(320, 1)
       auto wait_item = [&](uint32_t it) {
         return wait_bounded(bar(ctl.kv_full[it % C::kStages]), (it / C::kStages) & 1, wc);
       };
-      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uit) {
+      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
         const Unit w = unit_of(u, p);
         const int J = w.nblocks;
+        if (J == 0) continue;   // empty key range (split-KV)
         ok = wait_bounded(bar(ctl.q_full[0]), uit & 1, wc) &&
              wait_bounded(bar(ctl.q_full[1]), uit & 1, wc);
         if (!ok) break;
@@ -357,6 +382,7 @@ __global__ void __launch_bounds__(320, 1)
             }
           }
         }
+        ++uit;
       }
       // Every MMA issued must finish before TMEM is released.
       mma_commit(bar(ctl.drain));
@@ -374,9 +400,20 @@ __global__ void __launch_bounds__(320, 1)
     const float NEG_INF = __int_as_float(0xff800000);
     uint32_t sit = 0, uit = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uit) {
+    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
       const Unit w = unit_of(u, p);
       const int row = w.pair * 256 + t * 128 + r;
+      if (w.nblocks == 0) {
+        // Empty key range: O_part = 0 and lse_part = -inf (weight 0 in the merge).
+        if (row < p.N) {
+          const size_t prow = ((size_t)w.split * p.BH + w.bh) * p.N + row;
+          float4* dst = reinterpret_cast<float4*>(p.o_part + prow * D);
+#pragma unroll 4
+          for (int i = 0; i < D / 4; ++i) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+          p.lse_part[prow] = NEG_INF;
+        }
+        continue;
+      }
       const int lim_row = p.causal ? min(row, p.N - 1) : p.N - 1;   // last visible key
       const int lo_row = p.window > 0 ? row - p.window + 1 : 0;      // first visible key
       float m_ref = NEG_INF, ell = 0.0f;   // reference max (base 2), sum of f32 p
@@ -517,28 +554,49 @@ __global__ void __launch_bounds__(320, 1)
       else
         inv = (ell_r > 0.0f) ? 1.0f / ell_r : 0.0f;
       const bool live = row < p.N;
-      uint16_t* orow_g = reinterpret_cast<uint16_t*>(p.o) + ((size_t)w.bh * p.N + row) * D;
+      const float l2e = (ell > 0.0f) ? (m_ref + __log2f(ell)) * 0.69314718055994531f : NEG_INF;
+      if (p.o_part != nullptr) {
+        // Split-KV: this key range's O (normalised by its own sum) in fp32.
+        const size_t prow = ((size_t)w.split * p.BH + w.bh) * p.N + row;
+        float* orow_p = p.o_part + prow * D;
 #pragma unroll 1
-      for (int cc = 0; cc < D; cc += 32) {
-        uint32_t ov[32];
-        __syncwarp();
-        tmem_ld32(tO + cc, ov);
-        tmem_wait_ld();
-        reg_fence(ov);
-        uint32_t pk[16];
+        for (int cc = 0; cc < D; cc += 32) {
+          uint32_t ov[32];
+          __syncwarp();
+          tmem_ld32(tO + cc, ov);
+          tmem_wait_ld();
+          reg_fence(ov);
+          if (live) {
+            float4* dst = reinterpret_cast<float4*>(orow_p + cc);
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv, __uint_as_float(ov[2 * i + 1]) * inv);
-        if (live) {
-          uint4* dst = reinterpret_cast<uint4*>(orow_g + cc);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            for (int i = 0; i < 8; ++i)
+              dst[i] = make_float4(__uint_as_float(ov[4 * i]) * inv, __uint_as_float(ov[4 * i + 1]) * inv,
+                                   __uint_as_float(ov[4 * i + 2]) * inv, __uint_as_float(ov[4 * i + 3]) * inv);
+          }
         }
+        if (live) p.lse_part[prow] = l2e;
+      } else {
+        uint16_t* orow_g = reinterpret_cast<uint16_t*>(p.o) + ((size_t)w.bh * p.N + row) * D;
+#pragma unroll 1
+        for (int cc = 0; cc < D; cc += 32) {
+          uint32_t ov[32];
+          __syncwarp();
+          tmem_ld32(tO + cc, ov);
+          tmem_wait_ld();
+          reg_fence(ov);
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv, __uint_as_float(ov[2 * i + 1]) * inv);
+          if (live) {
+            uint4* dst = reinterpret_cast<uint4*>(orow_g + cc);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          }
+        }
+        if (live && p.lse != nullptr) p.lse[(size_t)w.bh * p.N + row] = l2e;
       }
-      if (live && p.lse != nullptr) {
-        const float l2e = (ell > 0.0f) ? (m_ref + __log2f(ell)) * 0.69314718055994531f : NEG_INF;
-        p.lse[(size_t)w.bh * p.N + row] = l2e;
-      }
+      ++uit;
       // The next unit's first P arrive (after this epilogue) releases O_t.
     }
   }

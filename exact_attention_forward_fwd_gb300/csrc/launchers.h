@@ -23,4 +23,9 @@ int status_attn_fp8_d128(bool clear);
 cudaError_t launch_fp8_prep(const void* x, void* x8, float* scales, const signed char* signs,
                             int BH, int H, int N, int transpose_out, cudaStream_t stream);
 
+// Split-KV merge of `splits` partial results ([splits][BH][N][D] fp32 O,
+// [splits][BH][N] lse) into O bf16 [BH][N][D] and lse [BH][N] (lse may be null).
+cudaError_t launch_splitkv_merge(const float* o_part, const float* lse_part, void* o, float* lse,
+                                 int splits, int BH, int N, int D, cudaStream_t stream);
+
 }  // namespace gb300

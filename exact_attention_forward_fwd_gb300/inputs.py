@@ -81,6 +81,10 @@ WORKLOADS = {
     # sliding window, the shape of the FA2/3 page's flash_attn_func example.
     "n8192_d128_gqa4_window4096": Workload("n8192_d128_gqa4_window4096", 2, 16, 8192, 128, True,
                                            seed=1006, H_kv=4, window=4096),
+    # One sequence of two heads: 64 query-tile pairs, fewer than the SMs of the
+    # device -- the shape split-KV (FlashDecoding-style key splitting) is for.
+    "n8192_d128_b1h2": Workload("n8192_d128_b1h2", 1, 2, 8192, 128, False, seed=1007),
+    "n8192_d128_b1h2_causal": Workload("n8192_d128_b1h2_causal", 1, 2, 8192, 128, True, seed=1007),
 }
 
 

@@ -31,6 +31,8 @@
 #ifndef GB300_ATTN_H
 #define GB300_ATTN_H
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -80,6 +82,47 @@ ATTN_API int attn_fwd(const void* q, const void* k, const void* v, void* o, floa
 ATTN_API int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                          int H, int H_kv, int N, int d, float scale, int causal, int window,
                          int dtype, attn_stream_t stream);
+
+/* Split-KV attention forward: the visible key blocks of every pair of 128-row
+ * query tiles are split into `num_splits` contiguous ranges, each a work unit
+ * of its own, so that shapes with few (batch, head, query tile) units still
+ * fill the device.  Each range writes its partial result -- O_s normalised by
+ * its own denominator, and its logsumexp L_s -- to the workspace; a merge
+ * kernel then computes, with M = max_s L_s,
+ *     O = sum_s exp(L_s - M) O_s / sum_s exp(L_s - M),
+ *     L = M + log sum_s exp(L_s - M),
+ * the rule for combining two blocks' (m, l, O) states ("FlashAttention-3 & GPU
+ * Kernel Optimization: Accelerating Transformer Attention", section "Online
+ * softmax tiling mathematics") applied along the key axis, as in FlashDecoding
+ * ("4.3 FlashAttention 2 & 3", section "Comparison, trade-offs, and when each
+ * wins", paragraph on decode).  A range with no visible key has weight 0.
+ *   q, k, v, o, lse, B, H, H_kv, N, d, scale, causal, window, dtype : as attn_fwd_ex.
+ *   num_splits : 1 .. 64 (more ranges than key blocks leaves some empty).
+ *   workspace  : caller-owned device scratch, 16-byte aligned, of at least
+ *                attn_splitkv_workspace_bytes(B, H, N, d, num_splits) bytes
+ *                (workspace_bytes says how large it is).  Overwritten entirely;
+ *                its initial contents do not matter.  Calls that share a
+ *                workspace must be ordered (the same stream, or synchronised).
+ * Errors: as attn_fwd_ex; ATTN_ERR_INVALID_ARG for num_splits out of range or a
+ * NULL or too small workspace; ATTN_ERR_ALIGNMENT for a workspace that is not
+ * 16-byte aligned. */
+ATTN_API int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                              int B, int H, int H_kv, int N, int d, float scale, int causal,
+                              int window, int dtype, int num_splits, void* workspace,
+                              size_t workspace_bytes, attn_stream_t stream);
+
+/* Workspace bytes attn_fwd_splitkv needs: the partial O (f32, num_splits * B *
+ * H * N * d values) and the partial logsumexp (f32, num_splits * B * H * N
+ * values), each rounded up to a multiple of 256 bytes; 0 for invalid arguments
+ * (B, H, N < 1, d not 64 or 128, num_splits outside 1 .. 64).  Host arithmetic. */
+ATTN_API size_t attn_splitkv_workspace_bytes(int B, int H, int N, int d, int num_splits);
+
+/* A split count that fills a device with num_sms SMs: 1 if the plain schedule
+ * has at least num_sms units; else the smallest count S (S <= 64 and S <=
+ * ceil(N / 128), the number of 128-key blocks) whose units * S work units fill
+ * at least 90% of the SM slots of the waves they take, or, if none does, the
+ * S that fills them best.  0 for invalid arguments.  Host arithmetic. */
+ATTN_API int attn_splitkv_default_splits(int B, int H, int N, int num_sms);
 
 /* Preparation of FP8 E4M3 operands with per-block scales and, optionally,
  * incoherent processing ("4.3 FlashAttention 2 & 3", section "Incoherent

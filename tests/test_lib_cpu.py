@@ -109,3 +109,49 @@ def test_product_path_has_no_cpu_fallback():
     q = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="CUDA tensor"):
         ga.attn_fwd(q, q, q)
+
+
+def test_splitkv_workspace_and_default_splits(L):
+    """Host arithmetic of the split-KV contract: workspace = partial O (f32) and
+    partial lse (f32), each rounded up to 256 bytes; the default split count is
+    the smallest that fills >= 90% of the SM slots of its waves (capped by the
+    128-key blocks and by 64), else the best-filling one."""
+    def ws(B, H, N, d, S):
+        rows = S * B * H * N
+        up = lambda x: (x + 255) // 256 * 256
+        return up(rows * d * 4) + up(rows * 4)
+    for args in [(1, 2, 256, 64, 3), (2, 16, 8192, 128, 1), (1, 1, 1, 128, 64), (3, 5, 77, 64, 7)]:
+        assert ga.splitkv_workspace_bytes(*args) == ws(*args), args
+    for bad in [(0, 1, 1, 64, 1), (1, 1, 1, 96, 1), (1, 1, 1, 64, 0), (1, 1, 1, 64, 65)]:
+        assert ga.splitkv_workspace_bytes(*bad) == 0, bad
+    def expect(B, H, N, sms):
+        u = B * H * ((N + 255) // 256)
+        if u >= sms:
+            return 1
+        fill = lambda S: u * S / (-(-u * S // sms) * sms)
+        cap = min(64, (N + 127) // 128)
+        for S in range(1, cap + 1):
+            if fill(S) >= 0.9:
+                return S
+        return max(range(1, cap + 1), key=lambda S: (fill(S), -S))
+    cases = [(2, 16, 8192, 152), (1, 2, 8192, 152), (1, 2, 256, 152), (1, 1, 32768, 152),
+             (1, 1, 16384, 1000), (1, 1, 16384, 10000), (3, 1, 1000, 152), (1, 3, 77, 152)]
+    for c in cases:
+        assert ga.splitkv_default_splits(*c) == expect(*c), c
+    assert ga.splitkv_default_splits(2, 16, 8192, 152) == 1      # 1024 units already
+    assert ga.splitkv_default_splits(1, 2, 8192, 152) == 7       # 64 units: 448 of 456 slots
+    assert ga.splitkv_default_splits(1, 2, 256, 152) == 2        # capped by 2 key blocks
+    assert ga.splitkv_default_splits(1, 1, 16384, 10000) == 64   # capped at 64
+    assert ga.splitkv_default_splits(0, 1, 1, 152) == 0
+
+
+def test_splitkv_validation_codes(L):
+    """Argument errors are reported before any device query."""
+    f = lambda S=2, ws=A, nbytes=1 << 30, d=128: L.attn_fwd_splitkv(
+        A, A, A, A, None, 1, 2, 2, 256, d, 0.1, 0, 0, 0, S, ws, nbytes, None)
+    assert f(S=0) == ga.ATTN_ERR_INVALID_ARG
+    assert f(S=65) == ga.ATTN_ERR_INVALID_ARG
+    assert f(ws=None) == ga.ATTN_ERR_INVALID_ARG
+    assert f(nbytes=ga.splitkv_workspace_bytes(1, 2, 256, 128, 2) - 1) == ga.ATTN_ERR_INVALID_ARG
+    assert f(ws=ctypes.c_void_p(A.value + 8)) == ga.ATTN_ERR_ALIGNMENT
+    assert f(d=96) == ga.ATTN_ERR_UNSUPPORTED
