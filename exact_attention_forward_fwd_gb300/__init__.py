@@ -11,6 +11,7 @@ Functions mirror the C entry points:
   attn_fwd(q, k, v, causal=False, scale=None, out=None, lse=None)
   attn_fwd_ex(q, k, v, causal=False, window=0, scale=None, ...)   (grouped KV heads, window)
   attn_fwd_splitkv(q, k, v, causal=False, window=0, num_splits=None, workspace=None, ...)
+  attn_fwd_splitkv_static(q, k, v, causal=False, window=0, num_splits=None, ...)  (no allocation)
   splitkv_workspace_bytes(B, H, N, d, num_splits), splitkv_default_splits(B, H, N, num_sms)
   fp8_prep(x, signs=None, transpose=False, out=None, scales=None)
   attn_fwd_fp8(q8, k8, v8t, q_scale, k_scale, v_scale, causal=False, scale=None, ...)
@@ -63,6 +64,7 @@ def lib() -> ctypes.CDLL:
     L.attn_grid_size.argtypes = [i, i, i, i]
     L.attn_fwd_splitkv.argtypes = [vp, vp, vp, vp, fp, i, i, i, i, i, f, i, i, i, i, vp,
                                    ctypes.c_size_t, vp]
+    L.attn_fwd_splitkv_static.argtypes = [vp, vp, vp, vp, fp, i, i, i, i, i, f, i, i, i, i, vp]
     L.attn_splitkv_workspace_bytes.argtypes = [i, i, i, i, i]
     L.attn_splitkv_workspace_bytes.restype = ctypes.c_size_t
     L.attn_splitkv_default_splits.argtypes = [i, i, i, i]
@@ -70,7 +72,7 @@ def lib() -> ctypes.CDLL:
     L.attn_status_str.restype = ctypes.c_char_p
     for name in ("attn_fwd", "attn_fwd_ex", "attn_fp8_prep", "attn_fwd_fp8", "attn_fwd_debug",
                  "attn_device_status", "attn_num_units", "attn_grid_size", "attn_fwd_splitkv",
-                 "attn_splitkv_default_splits"):
+                 "attn_fwd_splitkv_static", "attn_splitkv_default_splits"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -228,6 +230,38 @@ def attn_fwd_splitkv(q, k, v, causal: bool = False, window: int = 0, scale: floa
                                     int(num_splits), _ptr(workspace), workspace.numel(),
                                     _stream(q))
     _check(rc, "attn_fwd_splitkv")
+    return out, lse
+
+
+def attn_fwd_splitkv_static(q, k, v, causal: bool = False, window: int = 0,
+                            scale: float | None = None, num_splits: int | None = None, out=None,
+                            lse=None, return_lse: bool = True):
+    """attn_fwd_splitkv on the library's own 64 MiB scratch array: the C call
+    allocates nothing.  Calls must not overlap in time.  Returns (O, lse)."""
+    torch = _torch()
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, name, torch.bfloat16)
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q, k, v must be [B, H, N, d] / [B, H_kv, N, d]")
+    B, H, N, d = q.shape
+    H_kv = k.shape[1]
+    if tuple(k.shape) != (B, H_kv, N, d) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError(f"k and v must be [B, H_kv, N, d] = {(B, H_kv, N, d)}")
+    scale = d ** -0.5 if scale is None else scale
+    if num_splits is None:
+        sms = torch.cuda.get_device_properties(q.device).multi_processor_count
+        num_splits = splitkv_default_splits(B, H, N, sms)
+    out = torch.empty_like(q) if out is None else out
+    _need(out, "out", torch.bfloat16, q.shape)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, (B, H, N))
+    with torch.cuda.device(q.device):
+        rc = lib().attn_fwd_splitkv_static(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H,
+                                           H_kv, N, d, float(scale), int(bool(causal)),
+                                           int(window), ATTN_BF16, int(num_splits), _stream(q))
+    _check(rc, "attn_fwd_splitkv_static")
     return out, lse
 
 

@@ -6,6 +6,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
 #include "attn.h"
 #include "attn_kernel.cuh"
@@ -86,6 +87,27 @@ struct SplitArgs {
   size_t workspace_bytes = 0;
 };
 
+// Scratch of attn_fwd_splitkv_static: a file-scope device array (no allocation
+// call anywhere), its address looked up once per device.
+constexpr size_t kStaticScratchBytes = size_t(64) << 20;
+static __device__ __align__(256) unsigned char g_splitkv_scratch[kStaticScratchBytes];
+std::mutex g_scratch_mu;
+void* g_scratch_addr[64] = {};
+
+int static_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* a = nullptr;
+    if (cudaGetSymbolAddress(&a, g_splitkv_scratch) != cudaSuccess || a == nullptr)
+      return ATTN_ERR_CUDA;
+    g_scratch_addr[dev] = a;
+  }
+  *out = g_scratch_addr[dev];
+  return ATTN_OK;
+}
+
 int run_bf16(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
              int H_kv, int N, int d, float scale, int causal, int window, int dtype, int* status,
              unsigned long long timeout_ns, int skip_loads, cudaStream_t stream,
@@ -161,6 +183,25 @@ int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float
   split.splits = num_splits;
   split.workspace = workspace;
   split.workspace_bytes = workspace_bytes;
+  return run_bf16(q, k, v, o, lse, B, H, H_kv, N, d, scale, causal, window, dtype, nullptr,
+                  kDefaultTimeoutNs, 0, reinterpret_cast<cudaStream_t>(stream), split);
+}
+
+int attn_fwd_splitkv_static(const void* q, const void* k, const void* v, void* o, float* lse,
+                            int B, int H, int H_kv, int N, int d, float scale, int causal,
+                            int window, int dtype, int num_splits, attn_stream_t stream) {
+  if (num_splits < 1 || num_splits > kMaxSplits) return ATTN_ERR_INVALID_ARG;
+  SplitArgs split;
+  split.splits = num_splits;
+  const size_t need = attn_splitkv_workspace_bytes(B, H, N, d, num_splits);
+  if (need != 0) {
+    // Valid shape: the request must fit the static scratch.
+    if (need > kStaticScratchBytes) return ATTN_ERR_INVALID_ARG;
+    const int rc = static_scratch(&split.workspace);
+    if (rc) return rc;
+    split.workspace_bytes = kStaticScratchBytes;
+  }
+  // (need == 0: run_bf16 reports the argument error; it launches nothing.)
   return run_bf16(q, k, v, o, lse, B, H, H_kv, N, d, scale, causal, window, dtype, nullptr,
                   kDefaultTimeoutNs, 0, reinterpret_cast<cudaStream_t>(stream), split);
 }

@@ -111,6 +111,27 @@ ATTN_API int attn_fwd_splitkv(const void* q, const void* k, const void* v, void*
                               int window, int dtype, int num_splits, void* workspace,
                               size_t workspace_bytes, attn_stream_t stream);
 
+/* attn_fwd_splitkv without a caller workspace and without any allocation: the
+ * partial results go to one scratch array of 64 MiB (67108864 bytes) that the
+ * library defines as a file-scope device variable, so it exists on every
+ * device the library's code is loaded on.  The pages have no counterpart to
+ * this entry point; it serves callers that must not allocate, e.g. inside a
+ * captured CUDA graph.
+ *   Arguments and errors: as attn_fwd_splitkv, minus the workspace;
+ *   ATTN_ERR_INVALID_ARG also when attn_splitkv_workspace_bytes(B, H, N, d,
+ *   num_splits) exceeds 64 MiB (nothing is launched).
+ *   Nothing in the scratch needs to start at zero: every byte the merge reads
+ *   is written earlier in the same call.
+ *   Calls share the one array: two calls that overlap in time (different
+ *   streams or host threads without ordering) race and give undefined
+ *   results; order them.  The first call on each device looks the array's
+ *   address up (cudaGetSymbolAddress, ATTN_ERR_CUDA if that fails); make that
+ *   first call before capturing the stream into a graph. */
+ATTN_API int attn_fwd_splitkv_static(const void* q, const void* k, const void* v, void* o,
+                                     float* lse, int B, int H, int H_kv, int N, int d,
+                                     float scale, int causal, int window, int dtype,
+                                     int num_splits, attn_stream_t stream);
+
 /* Workspace bytes attn_fwd_splitkv needs: the partial O (f32, num_splits * B *
  * H * N * d values) and the partial logsumexp (f32, num_splits * B * H * N
  * values), each rounded up to a multiple of 256 bytes; 0 for invalid arguments
