@@ -1,4 +1,4 @@
-"""CPU oracle for the exact attention forward pass -- TEST INFRASTRUCTURE ONLY.
+"""CPU oracle for exact attention (forward and backward) -- TEST INFRASTRUCTURE ONLY.
 
 Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this package.  The product path (the C-ABI library and
@@ -15,9 +15,11 @@ Contents (all arithmetic in float64 unless a format fixes otherwise):
                 decode.
   fp8        -- incoherent processing (random-sign Hadamard rotation) and
                 per-128-row-block E4M3 quantisation of Q, K, V; dequantisation.
+  backward   -- gradients dQ, dK, dV of attention given dO: the chain rule
+                through the row softmax written out (the backward pass).
 
 Pins: every function here is checked by the ``-m "not gpu"`` tests against
 facts the source pages or mathematics fix (a printed worked example, closed
 forms, invariants, library routines).  No function is "parity unpinned".
 """
-from . import attention, e4m3, fp8, hadamard  # noqa: F401
+from . import attention, backward, e4m3, fp8, hadamard  # noqa: F401
