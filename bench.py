@@ -348,6 +348,37 @@ def run_mine(args):
                                  "frac": prep_bytes / (msprep * 1e-3) / 1e9 / peaks["hbm_gbs"]}}
         del fq, fk, fv, q8, k8, v8, of
 
+    # ------------------------------------------------------------ backward
+    # dQ, dK, dV of the benchmark workload (and its causal form) from the
+    # forward's O and lse; FLOPs by the page's convention, 2.5 x the forward
+    # (five 128x128 tile products per (query block, key block); the kernels do
+    # seven, recomputing S and dP for dQ instead of adding it atomically).
+    bwd = None
+    if not args.no_extra:
+        bwd = {"flops_convention": "2.5 x forward FLOPs (5 tile products); the kernels execute 7",
+               "l2": "Q, K, V, O, dO 320 MiB > 129 MB L2 (no flush)"}
+        g = torch.Generator().manual_seed(w.seed + 60)
+        dO = torch.randn(w.B, w.H, w.N, w.d, generator=g).to(torch.bfloat16).to(dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        wsb = torch.empty(ga.bwd_workspace_bytes(w.B, w.H, w.N, w.d), dtype=torch.uint8, device=dev)
+        for causal in (False, True):
+            ga.attn_fwd(q, k, v, causal=causal, scale=w.scale, out=o, lse=lse)
+            fb = lambda: ga.attn_bwd(q, k, v, o, lse, dO, causal=causal, scale=w.scale, dq=dq, dk=dk,
+                                     dv=dv, workspace=wsb)
+            for _ in range(args.warmup):
+                fb()
+            barrier()
+            msb = mor(_time_loop(fb, args.steps, stream))
+            fl = 2.5 * w.flops / (2 if causal else 1)
+            tb = fl / (msb * 1e-3) / 1e12
+            bwd["causal" if causal else "non_causal"] = {
+                "tflops": tb * ws, "ms": msb,
+                "roofline": {"bound": "tensor", "achieved": tb, "peak": peaks["bf16"], "unit": "TFLOP/s",
+                             "frac": tb / peaks["bf16"], "executed_frac": 1.4 * tb / peaks["bf16"]}}
+        if ga.device_status() != 0:
+            raise RuntimeError("kernel status word set during the backward benchmark")
+        del dO, dq, dk, dv, wsb
+
     # ------------------------------------------------------- other workloads
     others = {}
     if not args.no_extra:
@@ -421,6 +452,7 @@ def run_mine(args):
             "clocks": {k2: clocks[k2] for k2 in ("sm_mhz", "sm_max_mhz", "reasons")},
             "cpu_baseline": cpu,
             "fp8": fp8,
+            "backward": bwd,
             "workloads": others,
         }
         print(json.dumps(line))

@@ -13,6 +13,8 @@ Functions mirror the C entry points:
   attn_fwd_splitkv(q, k, v, causal=False, window=0, num_splits=None, workspace=None, ...)
   attn_fwd_splitkv_static(q, k, v, causal=False, window=0, num_splits=None, ...)  (no allocation)
   splitkv_workspace_bytes(B, H, N, d, num_splits), splitkv_default_splits(B, H, N, num_sms)
+  attn_bwd(q, k, v, o, lse, dO, causal=False, window=0, scale=None, ...)  -> (dq, dk, dv)
+  bwd_workspace_bytes(B, H, N, d)
   fp8_prep(x, signs=None, transpose=False, out=None, scales=None)
   attn_fwd_fp8(q8, k8, v8t, q_scale, k_scale, v_scale, causal=False, scale=None, ...)
   attn_fwd_fp8_from_bf16(q, k, v, signs, causal=False, scale=None)
@@ -65,6 +67,10 @@ def lib() -> ctypes.CDLL:
     L.attn_fwd_splitkv.argtypes = [vp, vp, vp, vp, fp, i, i, i, i, i, f, i, i, i, i, vp,
                                    ctypes.c_size_t, vp]
     L.attn_fwd_splitkv_static.argtypes = [vp, vp, vp, vp, fp, i, i, i, i, i, f, i, i, i, i, vp]
+    L.attn_bwd.argtypes = [vp, vp, vp, vp, fp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp,
+                           ctypes.c_size_t, vp]
+    L.attn_bwd_workspace_bytes.argtypes = [i, i, i, i]
+    L.attn_bwd_workspace_bytes.restype = ctypes.c_size_t
     L.attn_splitkv_workspace_bytes.argtypes = [i, i, i, i, i]
     L.attn_splitkv_workspace_bytes.restype = ctypes.c_size_t
     L.attn_splitkv_default_splits.argtypes = [i, i, i, i]
@@ -72,7 +78,7 @@ def lib() -> ctypes.CDLL:
     L.attn_status_str.restype = ctypes.c_char_p
     for name in ("attn_fwd", "attn_fwd_ex", "attn_fp8_prep", "attn_fwd_fp8", "attn_fwd_debug",
                  "attn_device_status", "attn_num_units", "attn_grid_size", "attn_fwd_splitkv",
-                 "attn_fwd_splitkv_static", "attn_splitkv_default_splits"):
+                 "attn_fwd_splitkv_static", "attn_splitkv_default_splits", "attn_bwd"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -263,6 +269,48 @@ def attn_fwd_splitkv_static(q, k, v, causal: bool = False, window: int = 0,
                                            int(window), ATTN_BF16, int(num_splits), _stream(q))
     _check(rc, "attn_fwd_splitkv_static")
     return out, lse
+
+
+def bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    """Bytes of device workspace attn_bwd needs (0 for invalid arguments)."""
+    return int(lib().attn_bwd_workspace_bytes(B, H, N, d))
+
+
+def attn_bwd(q, k, v, o, lse, dO, causal: bool = False, window: int = 0,
+             scale: float | None = None, dq=None, dk=None, dv=None, workspace=None):
+    """Gradients (dq, dk, dv) of attention given dO and the forward's o, lse.
+    k, v may have fewer heads than q (grouped KV heads)."""
+    torch = _torch()
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dO", dO)):
+        _need(t, name, torch.bfloat16)
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q, k, v must be [B, H, N, d] / [B, H_kv, N, d]")
+    B, H, N, d = q.shape
+    H_kv = k.shape[1]
+    if tuple(k.shape) != (B, H_kv, N, d) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError(f"k and v must be [B, H_kv, N, d] = {(B, H_kv, N, d)}")
+    for name, t in (("o", o), ("dO", dO)):
+        if tuple(t.shape) != tuple(q.shape):
+            raise ValueError(f"{name} must have the shape of q")
+    _need(lse, "lse", torch.float32, (B, H, N))
+    scale = d ** -0.5 if scale is None else scale
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _need(dq, "dq", torch.bfloat16, q.shape)
+    _need(dk, "dk", torch.bfloat16, k.shape)
+    _need(dv, "dv", torch.bfloat16, v.shape)
+    need = bwd_workspace_bytes(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    _need(workspace, "workspace", torch.uint8)
+    with torch.cuda.device(q.device):
+        rc = lib().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
+                            _ptr(dk), _ptr(dv), B, H, H_kv, N, d, float(scale),
+                            int(bool(causal)), int(window), _ptr(workspace), workspace.numel(),
+                            _stream(q))
+    _check(rc, "attn_bwd")
+    return dq, dk, dv
 
 
 def attn_fwd_debug(q, k, v, status, timeout_ns: int, skip_loads: int, causal: bool = False,

@@ -21,7 +21,7 @@ BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libgb300attn.so")
 
 SOURCES = ["attn_api.cu", "attn_bf16_d64.cu", "attn_bf16_d128.cu", "attn_fp8_d128.cu",
-           "fp8_prep.cu", "splitkv.cu"]
+           "fp8_prep.cu", "splitkv.cu", "attn_bwd.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler",
          "-fvisibility=hidden", "-I", INCLUDE, "-I", CSRC]

@@ -9,6 +9,7 @@
 #include <mutex>
 
 #include "attn.h"
+#include "attn_bwd.cuh"
 #include "attn_kernel.cuh"
 #include "launchers.h"
 #include "tmap.h"
@@ -232,6 +233,65 @@ int attn_splitkv_default_splits(int B, int H, int N, int num_sms) {
   return static_cast<int>(best);
 }
 
+size_t attn_bwd_workspace_bytes(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return 0;
+  const size_t rows = static_cast<size_t>(B) * H * ((static_cast<size_t>(N) + 127) / 128 * 128);
+  return 2 * round256(rows * sizeof(float));
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+             const void* dO, void* dq, void* dk, void* dv, int B, int H, int H_kv, int N, int d,
+             float scale, int causal, int window, void* workspace, size_t workspace_bytes,
+             attn_stream_t stream) {
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !workspace)
+    return ATTN_ERR_INVALID_ARG;
+  int rc = check_shape(B, H, N, scale, causal);
+  if (rc) return rc;
+  if (H_kv < 1 || H % H_kv != 0) return ATTN_ERR_INVALID_ARG;
+  if (window < 0 || (window > 0 && !causal)) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (workspace_bytes < attn_bwd_workspace_bytes(B, H, N, d)) return ATTN_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * H * ((N + 127) / 128) > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(dO, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) ||
+      !aligned(lse, 4) || !aligned(workspace, 16))
+    return ATTN_ERR_ALIGNMENT;
+  int sms = 0;
+  if ((rc = device_check(&sms))) return rc;
+  const int BH = B * H, BHk = B * H_kv;
+  CUtensorMap mq, mk, mv, mdo;
+  if (!encode_map_3d(&mq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, N, BH, 64, 128) ||
+      !encode_map_3d(&mk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, N, BHk, 64, 128) ||
+      !encode_map_3d(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, N, BHk, 64, 128) ||
+      !encode_map_3d(&mdo, dO, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, N, BH, 64, 128))
+    return ATTN_ERR_CUDA;
+  BwdParams p{};
+  p.N = N;
+  p.Npad = (N + 127) / 128 * 128;
+  const size_t half = round256(static_cast<size_t>(BH) * p.Npad * sizeof(float));
+  float* lp = static_cast<float*>(workspace);
+  float* dd = reinterpret_cast<float*>(static_cast<char*>(workspace) + half);
+  p.lp = lp;
+  p.dd = dd;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.BH = BH;
+  p.BHk = BHk;
+  p.H = H;
+  p.Hk = H_kv;
+  p.group = H / H_kv;
+  p.window = window;
+  p.causal = causal;
+  p.nb = (N + 127) / 128;
+  p.scale = scale;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.timeout_ns = kDefaultTimeoutNs;
+  cudaError_t e = launch_attn_bwd(d, mq, mk, mv, mdo, p, o, dO, lse, lp, dd, sms,
+                                  reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 int attn_fwd_debug(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                    int N, int d, float scale, int causal, int* dev_status,
                    unsigned long long timeout_ns, int skip_loads, attn_stream_t stream) {
@@ -289,9 +349,9 @@ int attn_fwd_fp8(const void* q8, const void* k8, const void* v8t, const float* q
 int attn_device_status(int clear) {
   if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_ERR_CUDA;
   int out = ATTN_OK;
-  const int s[3] = {status_attn_bf16_d64(clear != 0), status_attn_bf16_d128(clear != 0),
-                    status_attn_fp8_d128(clear != 0)};
-  for (int i = 0; i < 3; ++i)
+  const int s[4] = {status_attn_bf16_d64(clear != 0), status_attn_bf16_d128(clear != 0),
+                    status_attn_fp8_d128(clear != 0), status_attn_bwd(clear != 0)};
+  for (int i = 0; i < 4; ++i)
     if (s[i] != 0 && out == ATTN_OK) out = s[i];
   return out;
 }

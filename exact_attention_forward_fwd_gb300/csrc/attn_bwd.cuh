@@ -1,0 +1,712 @@
+// Exact attention backward for sm_103a: dQ, dK, dV of O = softmax(scale Q K^T
+// [+mask]) V given dO, the forward's O and its logsumexp L.
+//
+// Method ("4.3 FlashAttention 2 & 3: Work Partitioning, Warp Specialization &
+// FP8", section "The backward pass: recompute, and the one identity that makes
+// it tile-able"; "Learn: The Memory Wall & FlashAttention", section 5.3):
+//   * S and P are recomputed tile by tile, never stored: P_ij = exp(S_ij - L_i);
+//   * D_i = rowdot(dO_i, O_i) is computed once by a small preprocessing kernel;
+//   * dV = P^T dO, dP = dO V^T, dS = P o (dP - D), dQ = scale dS K,
+//     dK = scale dS^T Q;
+//   * dK, dV are reductions over query blocks: one work unit owns a key block
+//     and loops over the query blocks that see it, so they accumulate locally.
+//     dQ, the reduction over key blocks, is computed by a second kernel that
+//     owns a query block and loops over key blocks -- the "separate pass" the
+//     page names as the alternative to atomic adds -- so the result is
+//     deterministic.  That recomputes S and dP once more (7 tile products per
+//     (query block, key block) instead of 5).
+//
+// Blackwell mapping (this file's own design), both kernels one persistent CTA
+// per SM, 320 threads: warps 0-7 element-wise work (warp w owns TMEM lane
+// quarter w & 3 and half w >> 2 of the tile's columns), warp 8 TMA, warp 9
+// TMEM allocation and every tcgen05.mma from one thread.
+//   dK/dV kernel (keys on the TMEM lanes): S^T = K Q^T and dP^T = V dO^T (SS);
+//     P^T (bf16) over S^T, dS^T (bf16) over dP^T; dV += P^T dO and
+//     dK += dS^T Q (TS, P^T / dS^T straight from TMEM, Q and dO as MN-major
+//     B operands -- the tiles TMA loaded for the SS products).  TMEM: S^T
+//     [0,128), dP^T [128,256), dV [256,256+D), dK [256+D,256+2D).  The
+//     element-wise pass first writes P^T (dV can start) and then dS^T.
+//   dQ kernel (queries on the lanes, L and D per thread): S = Q K^T into one of
+//     two buffers [0,128) / [384,512), dP = dO V^T [128,256), dS (bf16) over S,
+//     dQ += dS K (TS, K as MN-major B) [256,256+D).  S(j+1) runs during the
+//     element-wise pass of block j.
+// Every wait is bounded (status word + abort flag, as in the forward).
+#pragma once
+
+#include "attn_kernel.cuh"
+
+namespace gb300 {
+
+struct BwdParams {
+  const float* lp;       // [BH][Npad] L * log2(e) (+inf past N)
+  const float* dd;       // [BH][Npad] D = rowdot(dO, O) (0 past N)
+  void* dq;              // bf16 [BH][N][D]
+  void* dk;              // bf16 [BHk][N][D]
+  void* dv;              // bf16 [BHk][N][D]
+  int* status;           // device status word, or null for the library's own word
+  int N, Npad;           // sequence length; N rounded up to 128
+  int BH, BHk, H, Hk;    // batch * query heads, batch * KV heads, heads per batch
+  int group;             // query heads per KV head
+  int window, causal;
+  int nb;                // ceil(N / 128): query blocks == key blocks
+  int num_units;
+  float scale_log2;      // scale * log2(e)
+  float scale;
+  unsigned long long timeout_ns;
+};
+
+template <int D>
+struct BCfg {
+  static_assert(D == 64 || D == 128, "head dim 64 or 128");
+  static constexpr int kTile = 128 * D * 2;                 // 128 rows x D bf16
+  static constexpr int kSlabs = D / 64;                     // 128-byte column slabs
+  static constexpr int kStages = (D == 128) ? 5 : 10;       // ring of tiles
+  static constexpr int kSmemBytes = (2 + kStages) * kTile + 1024;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr int kThreads = 320;
+  static constexpr int kSSteps = D / 16;                    // K = D for S, dP
+  static constexpr uint32_t kIdescSS = make_idesc(128, 128, 1, 1, false, false);
+  static constexpr uint32_t kIdescTS = make_idesc(128, D, 1, 1, false, true);
+};
+
+struct BwdCtl {
+  uint64_t full[16];       // ring slot loaded
+  uint64_t empty[16];      // ring slot free
+  uint64_t fix_full;       // the unit's fixed tiles (K, V or Q, dO) loaded
+  uint64_t fix_empty;      // ... free again
+  uint64_t s_full;         // S and dP of a block computed
+  uint64_t p_ready;        // dK/dV: P^T written; dQ: dS written (8 warp arrivals)
+  uint64_t ds_ready;       // dK/dV: dS^T written (8 warp arrivals)
+  uint64_t unit_done;      // the unit's accumulators final
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+// Query blocks [i_lo, i_hi] that see key block j.
+__device__ __forceinline__ void bwd_qrange(int j, const BwdParams& p, int& i_lo, int& i_hi) {
+  i_lo = p.causal ? j : 0;
+  i_hi = p.nb - 1;
+  if (p.window > 0) i_hi = min(i_hi, (j * 128 + 126 + p.window) / 128);
+}
+
+// Key blocks [j_lo, j_hi] that query block i sees.
+__device__ __forceinline__ void bwd_krange(int i, const BwdParams& p, int& j_lo, int& j_hi) {
+  j_hi = p.causal ? i : p.nb - 1;
+  j_lo = p.window > 0 ? max(0, i * 128 - p.window + 1) / 128 : 0;
+}
+
+// Element (key k, query q) visible under the mask (k, q global; q < N assumed).
+__device__ __forceinline__ bool bwd_visible(int k, int q, const BwdParams& p) {
+  return k < p.N && (!p.causal || k <= q) && (p.window <= 0 || k > q - p.window);
+}
+
+// ============================================================================
+// dK, dV: one unit = (batch * KV head, 128-key block j).
+// ============================================================================
+template <int D>
+__global__ void __launch_bounds__(320, 1)
+    attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                         const BwdParams p) {
+  using C = BCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ BwdCtl ctl;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sK = smem_addr(smem);
+  const uint32_t sV = sK + C::kTile;
+  const uint32_t sRing = sV + C::kTile;     // Q_i / dO_i tiles, alternating
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  auto bar = [&](uint64_t& b) { return smem_addr(&b); };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(bar(ctl.full[s]), 1);
+      mbar_init(bar(ctl.empty[s]), 1);
+    }
+    mbar_init(bar(ctl.fix_full), 1);
+    mbar_init(bar(ctl.fix_empty), 1);
+    mbar_init(bar(ctl.s_full), 1);
+    mbar_init(bar(ctl.p_ready), 8);
+    mbar_init(bar(ctl.ds_ready), 8);
+    mbar_init(bar(ctl.unit_done), 1);
+    mbar_init(bar(ctl.drain), 1);
+    ctl.abort_flag = 0;
+    fence_mbarrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_addr(&ctl.tmem_base), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl.tmem_base;
+  const WaitCtx wc{&ctl.abort_flag, p.status ? p.status : &g_attn_status, p.timeout_ns};
+
+  // Unit u -> (bhk, j).  Causal: ascending j (key block 0 sees the most query
+  // blocks) across all heads first; otherwise the key blocks of one head in turn.
+  auto unit = [&](int u, int& bhk, int& j) {
+    if (p.causal) {
+      j = u / p.BHk;
+      bhk = u - j * p.BHk;
+    } else {
+      bhk = u / p.nb;
+      j = u - bhk * p.nb;
+    }
+  };
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tensormap(&tmQ);
+      prefetch_tensormap(&tmK);
+      prefetch_tensormap(&tmV);
+      prefetch_tensormap(&tmdO);
+      const uint64_t pol_fix = l2_policy_evict_first();
+      const uint64_t pol_ring = l2_policy_evict_last();
+      uint32_t item = 0, uit = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uit) {
+        int bhk, j;
+        unit(u, bhk, j);
+        int i_lo, i_hi;
+        bwd_qrange(j, p, i_lo, i_hi);
+        const int nI = i_hi - i_lo + 1;
+        const int b = bhk / p.Hk, g = bhk - (bhk / p.Hk) * p.Hk;
+        if (uit > 0 && !(ok = wait_bounded(bar(ctl.fix_empty), (uit - 1) & 1, wc))) break;
+        mbar_arrive_expect_tx(bar(ctl.fix_full), 2 * C::kTile);
+        for (int s = 0; s < C::kSlabs; ++s) {
+          tma_load_3d_hint(sK + s * 16384, &tmK, bar(ctl.fix_full), s * 64, j * 128, bhk, pol_fix);
+          tma_load_3d_hint(sV + s * 16384, &tmV, bar(ctl.fix_full), s * 64, j * 128, bhk, pol_fix);
+        }
+        for (int t = 0; t < p.group * nI && ok; ++t) {
+          const int hh = t / nI, i = i_lo + (t - hh * nI);
+          const int bh = b * p.H + g * p.group + hh;
+          for (int w2 = 0; w2 < 2 && ok; ++w2, ++item) {   // Q_i, then dO_i
+            const uint32_t slot = item % C::kStages;
+            if (!(ok = wait_bounded(bar(ctl.empty[slot]), ((item / C::kStages) & 1) ^ 1, wc))) break;
+            mbar_arrive_expect_tx(bar(ctl.full[slot]), C::kTile);
+            for (int s = 0; s < C::kSlabs; ++s)
+              tma_load_3d_hint(sRing + slot * C::kTile + s * 16384, w2 == 0 ? &tmQ : &tmdO,
+                               bar(ctl.full[slot]), s * 64, i * 128, bh, pol_ring);
+          }
+        }
+      }
+      // Let every copy started land before the CTA can exit.
+      const uint32_t issued = item;
+      for (uint32_t s = 0; s < (uint32_t)C::kStages && s < issued; ++s) {
+        const uint32_t last = s + ((issued - 1 - s) / C::kStages) * C::kStages;
+        wait_bounded(bar(ctl.full[s]), (last / C::kStages) & 1, wc, false);
+      }
+      if (uit > 0) wait_bounded(bar(ctl.fix_full), (uit - 1) & 1, wc, false);
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t item = 0, uit = 0, gblk = 0;
+      bool ok = true;
+      auto wait_slot = [&](uint32_t it) {
+        return wait_bounded(bar(ctl.full[it % C::kStages]), (it / C::kStages) & 1, wc);
+      };
+      // SS product [M = 128 rows of a] x [N = 128 rows of b]^T over K = D.
+      auto ss = [&](uint32_t d_col, uint32_t a0, uint32_t b0) {
+#pragma unroll
+        for (int k = 0; k < C::kSSteps; ++k) {
+          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+          mma_f16_ss(tmem + d_col, make_smem_desc(a0 + off, 16, 1024, kSwizzle128B),
+                     make_smem_desc(b0 + off, 16, 1024, kSwizzle128B), C::kIdescSS, k > 0);
+        }
+      };
+      // TS product: A = 128 x 128 bf16 in TMEM (queries [0,64) at a_col,
+      // [64,128) at a_col + 64), B = a [queries x D] tile as MN-major operand.
+      auto ts = [&](uint32_t d_col, uint32_t a_col, uint32_t b0, bool acc) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t a = tmem + a_col + (k >> 2) * 64 + (k & 3) * 8;
+          mma_f16_ts(tmem + d_col, a, make_smem_desc(b0 + k * 2048, 16384, 1024, kSwizzle128B),
+                     C::kIdescTS, (acc || k > 0) ? 1u : 0u);
+        }
+      };
+      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uit) {
+        int bhk, j;
+        unit(u, bhk, j);
+        int i_lo, i_hi;
+        bwd_qrange(j, p, i_lo, i_hi);
+        const int T = p.group * (i_hi - i_lo + 1);
+        if (!(ok = wait_bounded(bar(ctl.fix_full), uit & 1, wc))) break;
+        // Block t: Q item = base + 2t, dO item = base + 2t + 1.
+        const uint32_t base = item;
+        item += 2 * T;
+        // prologue: S^T(0), dP^T(0)
+        if (!(ok = wait_slot(base) && wait_slot(base + 1))) break;
+        tc_fence_after();
+        ss(0, sK, sRing + (base % C::kStages) * C::kTile);
+        ss(128, sV, sRing + ((base + 1) % C::kStages) * C::kTile);
+        mma_commit(bar(ctl.s_full));
+        for (int t = 0; t < T && ok; ++t, ++gblk) {
+          const uint32_t iq = base + 2 * t, io = iq + 1;
+          const uint32_t sQ = sRing + (iq % C::kStages) * C::kTile;
+          const uint32_t sdO = sRing + (io % C::kStages) * C::kTile;
+          // dV += P^T dO once P^T is written
+          if (!(ok = wait_bounded(bar(ctl.p_ready), gblk & 1, wc))) break;
+          tc_fence_after();
+          ts(256, 0, sdO, t > 0);
+          mma_commit(bar(ctl.empty[io % C::kStages]));    // dO_i done (dP^T(t) was earlier)
+          // S^T(t+1): the S^T columns are free once dV(t) has read P^T
+          const bool more = t + 1 < T;
+          if (more) {
+            if (!(ok = wait_slot(iq + 2))) break;
+            tc_fence_after();
+            ss(0, sK, sRing + ((iq + 2) % C::kStages) * C::kTile);
+          }
+          // dK += dS^T Q once dS^T is written
+          if (!(ok = wait_bounded(bar(ctl.ds_ready), gblk & 1, wc))) break;
+          tc_fence_after();
+          ts(256 + D, 128, sQ, t > 0);
+          mma_commit(bar(ctl.empty[iq % C::kStages]));    // Q_i done
+          if (more) {
+            if (!(ok = wait_slot(io + 2))) break;
+            tc_fence_after();
+            ss(128, sV, sRing + ((io + 2) % C::kStages) * C::kTile);
+            mma_commit(bar(ctl.s_full));
+          }
+        }
+        mma_commit(bar(ctl.unit_done));
+        mma_commit(bar(ctl.fix_empty));
+      }
+      mma_commit(bar(ctl.drain));
+      wait_bounded(bar(ctl.drain), 0, wc, false);
+    }
+  } else {
+    // ------------------------------------------------------------ element-wise
+    const int qd = warp & 3;             // TMEM lane quarter: keys 32qd .. 32qd+31
+    const int h = warp >> 2;             // queries [64h, 64h+64) of each block
+    const int r = qd * 32 + lane;        // key row within the block
+    const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
+    const float cl = p.scale_log2;
+    uint32_t uit = 0, gblk = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uit) {
+      int bhk, j;
+      unit(u, bhk, j);
+      int i_lo, i_hi;
+      bwd_qrange(j, p, i_lo, i_hi);
+      const int nI = i_hi - i_lo + 1;
+      const int b = bhk / p.Hk, g = bhk - (bhk / p.Hk) * p.Hk;
+      const int key = j * 128 + r;
+      for (int t = 0; t < p.group * nI; ++t, ++gblk) {
+        const int hh = t / nI, i = i_lo + (t - hh * nI);
+        const int bh = b * p.H + g * p.group + hh;
+        const int q0 = i * 128 + 64 * h;   // first query of this thread's columns
+        // Mask needed unless every (key, query) of the block is visible.
+        const bool full_vis = (!p.causal || j * 128 + 127 <= i * 128) &&
+                              (p.window <= 0 || j * 128 > i * 128 + 127 - p.window);
+        ok = wait_bounded(bar(ctl.s_full), gblk & 1, wc);
+        ok = __all_sync(0xffffffffu, ok);
+        ok = bar_and(1, 256, ok);
+        if (!ok) break;
+        tc_fence_after();
+        const float4* lq = reinterpret_cast<const float4*>(p.lp + (size_t)bh * p.Npad + q0);
+        const float4* dq4 = reinterpret_cast<const float4*>(p.dd + (size_t)bh * p.Npad + q0);
+        // ---- phase A: P^T = exp2(S^T * c - L') for this thread's 64 queries
+        float pr[64];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t sv[32];
+          tmem_ld32(tmem + lane_off + 64 * h + 32 * c, sv);
+          tmem_wait_ld();
+          reg_fence(sv);
+          uint32_t pk[16];
+#pragma unroll
+          for (int v4 = 0; v4 < 8; ++v4) {
+            const float4 L = __ldg(lq + 8 * c + v4);
+            const float Ls[4] = {L.x, L.y, L.z, L.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int col = 32 * c + 4 * v4 + e;
+              float pv = ex2_approx(fmaf(__uint_as_float(sv[4 * v4 + e]), cl, -Ls[e]));
+              if (!full_vis && !bwd_visible(key, q0 + col, p)) pv = 0.0f;
+              pr[col] = pv;
+            }
+          }
+#pragma unroll
+          for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(pr[32 * c + 2 * e], pr[32 * c + 2 * e + 1]);
+          // P^T of queries [64h + 32c, +32) -> columns [64h + 16c, +16): inside the
+          // S^T columns this thread has already read.
+          tmem_st16(tmem + lane_off + 64 * h + 16 * c, pk);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(ctl.p_ready));
+        // ---- phase B: dS^T = P^T o (dP^T - D)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t dv[32];
+          tmem_ld32(tmem + lane_off + 128 + 64 * h + 32 * c, dv);
+          tmem_wait_ld();
+          reg_fence(dv);
+          uint32_t pk[16];
+#pragma unroll
+          for (int v4 = 0; v4 < 8; ++v4) {
+            const float4 Dv = __ldg(dq4 + 8 * c + v4);
+            const float Ds[4] = {Dv.x, Dv.y, Dv.z, Dv.w};
+            float ds[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              ds[e] = pr[32 * c + 4 * v4 + e] * (__uint_as_float(dv[4 * v4 + e]) - Ds[e]);
+            pk[2 * v4] = pack_bf16x2(ds[0], ds[1]);
+            pk[2 * v4 + 1] = pack_bf16x2(ds[2], ds[3]);
+          }
+          tmem_st16(tmem + lane_off + 128 + 64 * h + 16 * c, pk);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(ctl.ds_ready));
+      }
+      if (!ok) break;
+      // ---------------------------------------------------------- epilogue
+      ok = wait_bounded(bar(ctl.unit_done), uit & 1, wc);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const bool live = key < p.N;
+      const size_t orow = ((size_t)bhk * p.N + key) * D + (D / 2) * h;
+#pragma unroll 1
+      for (int which = 0; which < 2; ++which) {   // dV, then dK (times scale)
+        const float mul = which == 0 ? 1.0f : p.scale;
+        uint16_t* dst_row = reinterpret_cast<uint16_t*>(which == 0 ? p.dv : p.dk) + orow;
+#pragma unroll 1
+        for (int cc = 0; cc < D / 2; cc += 32) {
+          uint32_t av[32];
+          __syncwarp();
+          tmem_ld32(tmem + lane_off + 256 + which * D + (D / 2) * h + cc, av);
+          tmem_wait_ld();
+          reg_fence(av);
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            pk[e] = pack_bf16x2(__uint_as_float(av[2 * e]) * mul, __uint_as_float(av[2 * e + 1]) * mul);
+          if (live) {
+            uint4* dst = reinterpret_cast<uint4*>(dst_row + cc);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+          }
+        }
+      }
+      tc_fence_before();   // accumulators read: the next unit's first products may overwrite them
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 9) tmem_dealloc(tmem, C::kTmemCols);
+}
+
+// ============================================================================
+// dQ: one unit = (batch * query head, 128-query block i).
+// ============================================================================
+template <int D>
+__global__ void __launch_bounds__(320, 1)
+    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                       const BwdParams p) {
+  using C = BCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ BwdCtl ctl;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sQ = smem_addr(smem);
+  const uint32_t sdO = sQ + C::kTile;
+  const uint32_t sRing = sdO + C::kTile;    // K_j / V_j tiles, alternating
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  auto bar = [&](uint64_t& b) { return smem_addr(&b); };
+  constexpr uint32_t kColDP = 128, kColDQ = 256, kColS1 = 384;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(bar(ctl.full[s]), 1);
+      mbar_init(bar(ctl.empty[s]), 1);
+    }
+    mbar_init(bar(ctl.fix_full), 1);
+    mbar_init(bar(ctl.fix_empty), 1);
+    mbar_init(bar(ctl.s_full), 1);
+    mbar_init(bar(ctl.p_ready), 8);
+    mbar_init(bar(ctl.ds_ready), 8);
+    mbar_init(bar(ctl.unit_done), 1);
+    mbar_init(bar(ctl.drain), 1);
+    ctl.abort_flag = 0;
+    fence_mbarrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_addr(&ctl.tmem_base), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl.tmem_base;
+  const WaitCtx wc{&ctl.abort_flag, p.status ? p.status : &g_attn_status, p.timeout_ns};
+
+  // Unit u -> (bh, i).  Causal: longest first (last query blocks of all heads).
+  auto unit = [&](int u, int& bh, int& i) {
+    if (p.causal) {
+      const int rr = u / p.BH;
+      bh = u - rr * p.BH;
+      i = p.nb - 1 - rr;
+    } else {
+      bh = u / p.nb;
+      i = u - bh * p.nb;
+    }
+  };
+  auto kv_head = [&](int bh) {
+    const int b = bh / p.H, hq = bh - (bh / p.H) * p.H;
+    return b * p.Hk + hq / p.group;
+  };
+  auto sbuf = [&](uint32_t gg) { return (gg & 1) ? kColS1 : 0u; };
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tensormap(&tmQ);
+      prefetch_tensormap(&tmK);
+      prefetch_tensormap(&tmV);
+      prefetch_tensormap(&tmdO);
+      const uint64_t pol_fix = l2_policy_evict_first();
+      const uint64_t pol_ring = l2_policy_evict_last();
+      uint32_t item = 0, uit = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uit) {
+        int bh, i;
+        unit(u, bh, i);
+        int j_lo, j_hi;
+        bwd_krange(i, p, j_lo, j_hi);
+        const int bhk = kv_head(bh);
+        if (uit > 0 && !(ok = wait_bounded(bar(ctl.fix_empty), (uit - 1) & 1, wc))) break;
+        mbar_arrive_expect_tx(bar(ctl.fix_full), 2 * C::kTile);
+        for (int s = 0; s < C::kSlabs; ++s) {
+          tma_load_3d_hint(sQ + s * 16384, &tmQ, bar(ctl.fix_full), s * 64, i * 128, bh, pol_fix);
+          tma_load_3d_hint(sdO + s * 16384, &tmdO, bar(ctl.fix_full), s * 64, i * 128, bh, pol_fix);
+        }
+        for (int jj = j_lo; jj <= j_hi && ok; ++jj) {
+          for (int w2 = 0; w2 < 2 && ok; ++w2, ++item) {   // K_j, then V_j
+            const uint32_t slot = item % C::kStages;
+            if (!(ok = wait_bounded(bar(ctl.empty[slot]), ((item / C::kStages) & 1) ^ 1, wc))) break;
+            mbar_arrive_expect_tx(bar(ctl.full[slot]), C::kTile);
+            for (int s = 0; s < C::kSlabs; ++s)
+              tma_load_3d_hint(sRing + slot * C::kTile + s * 16384, w2 == 0 ? &tmK : &tmV,
+                               bar(ctl.full[slot]), s * 64, jj * 128, bhk, pol_ring);
+          }
+        }
+      }
+      const uint32_t issued = item;
+      for (uint32_t s = 0; s < (uint32_t)C::kStages && s < issued; ++s) {
+        const uint32_t last = s + ((issued - 1 - s) / C::kStages) * C::kStages;
+        wait_bounded(bar(ctl.full[s]), (last / C::kStages) & 1, wc, false);
+      }
+      if (uit > 0) wait_bounded(bar(ctl.fix_full), (uit - 1) & 1, wc, false);
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t item = 0, uit = 0, gblk = 0;
+      bool ok = true;
+      auto wait_slot = [&](uint32_t it) {
+        return wait_bounded(bar(ctl.full[it % C::kStages]), (it / C::kStages) & 1, wc);
+      };
+      auto ss = [&](uint32_t d_col, uint32_t a0, uint32_t b0) {
+#pragma unroll
+        for (int k = 0; k < C::kSSteps; ++k) {
+          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+          mma_f16_ss(tmem + d_col, make_smem_desc(a0 + off, 16, 1024, kSwizzle128B),
+                     make_smem_desc(b0 + off, 16, 1024, kSwizzle128B), C::kIdescSS, k > 0);
+        }
+      };
+      auto slot_addr = [&](uint32_t it) { return sRing + (it % C::kStages) * C::kTile; };
+      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uit) {
+        int bh, i;
+        unit(u, bh, i);
+        int j_lo, j_hi;
+        bwd_krange(i, p, j_lo, j_hi);
+        const int J = j_hi - j_lo + 1;
+        if (!(ok = wait_bounded(bar(ctl.fix_full), uit & 1, wc))) break;
+        const uint32_t base = item;            // K_j item = base + 2jj, V_j = base + 2jj + 1
+        item += 2 * J;
+        const uint32_t g0 = gblk;
+        // prologue: S(0), dP(0)
+        if (!(ok = wait_slot(base) && wait_slot(base + 1))) break;
+        tc_fence_after();
+        ss(sbuf(g0), sQ, slot_addr(base));
+        ss(kColDP, sdO, slot_addr(base + 1));
+        mma_commit(bar(ctl.s_full));
+        mma_commit(bar(ctl.empty[(base + 1) % C::kStages]));   // V_0 done
+        for (int jj = 0; jj < J && ok; ++jj, ++gblk) {
+          const uint32_t ik = base + 2 * jj;
+          const bool more = jj + 1 < J;
+          // S(jj+1) into the other buffer while the element-wise pass of jj runs
+          if (more) {
+            if (!(ok = wait_slot(ik + 2))) break;
+            tc_fence_after();
+            ss(sbuf(gblk + 1), sQ, slot_addr(ik + 2));
+          }
+          if (!(ok = wait_bounded(bar(ctl.p_ready), gblk & 1, wc))) break;
+          tc_fence_after();
+          // dP(jj+1): the dP columns were read by the element-wise pass of jj
+          if (more) {
+            if (!(ok = wait_slot(ik + 3))) break;
+            tc_fence_after();
+            ss(kColDP, sdO, slot_addr(ik + 3));
+            mma_commit(bar(ctl.s_full));
+            mma_commit(bar(ctl.empty[(ik + 3) % C::kStages]));   // V_{jj+1} done
+          }
+          // dQ += dS K_j (K_j as MN-major B)
+          const uint32_t a_col = sbuf(gblk);
+          const uint32_t kb = slot_addr(ik);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t a = tmem + a_col + (k >> 2) * 64 + (k & 3) * 8;
+            mma_f16_ts(tmem + kColDQ, a, make_smem_desc(kb + k * 2048, 16384, 1024, kSwizzle128B),
+                       C::kIdescTS, (jj > 0 || k > 0) ? 1u : 0u);
+          }
+          mma_commit(bar(ctl.empty[ik % C::kStages]));   // K_j done
+        }
+        mma_commit(bar(ctl.unit_done));
+        mma_commit(bar(ctl.fix_empty));
+      }
+      mma_commit(bar(ctl.drain));
+      wait_bounded(bar(ctl.drain), 0, wc, false);
+    }
+  } else {
+    // ------------------------------------------------------------ element-wise
+    const int qd = warp & 3;             // TMEM lane quarter: queries 32qd .. 32qd+31
+    const int h = warp >> 2;             // keys [64h, 64h+64) of each block
+    const int r = qd * 32 + lane;        // query row within the block
+    const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
+    const float cl = p.scale_log2;
+    uint32_t uit = 0, gblk = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uit) {
+      int bh, i;
+      unit(u, bh, i);
+      int j_lo, j_hi;
+      bwd_krange(i, p, j_lo, j_hi);
+      const int q = i * 128 + r;
+      const float Lq = __ldg(p.lp + (size_t)bh * p.Npad + q);   // +inf past N: P = 0
+      const float Dq = __ldg(p.dd + (size_t)bh * p.Npad + q);
+      for (int jj = j_lo; jj <= j_hi; ++jj, ++gblk) {
+        const bool full_vis = (jj * 128 + 127 < p.N) && (!p.causal || jj * 128 + 127 <= i * 128) &&
+                              (p.window <= 0 || jj * 128 > i * 128 + 127 - p.window);
+        ok = wait_bounded(bar(ctl.s_full), gblk & 1, wc);
+        ok = __all_sync(0xffffffffu, ok);
+        ok = bar_and(1, 256, ok);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t scol = sbuf(gblk) + 64 * h;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t sv[32], dv[32];
+          tmem_ld32(tmem + lane_off + scol + 32 * c, sv);
+          tmem_ld32(tmem + lane_off + kColDP + 64 * h + 32 * c, dv);
+          tmem_wait_ld();
+          reg_fence(sv);
+          reg_fence(dv);
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            float ds2[2];
+#pragma unroll
+            for (int z = 0; z < 2; ++z) {
+              const int col = 2 * e + z;
+              float pv = ex2_approx(fmaf(__uint_as_float(sv[col]), cl, -Lq));
+              if (!full_vis && !bwd_visible(jj * 128 + 64 * h + 32 * c + col, q, p)) pv = 0.0f;
+              ds2[z] = pv * (__uint_as_float(dv[col]) - Dq);
+            }
+            pk[e] = pack_bf16x2(ds2[0], ds2[1]);
+          }
+          // dS of keys [64h + 32c, +32) -> columns [64h + 16c, +16) of this S buffer
+          tmem_st16(tmem + lane_off + scol + 16 * c, pk);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(ctl.p_ready));
+      }
+      if (!ok) break;
+      // ---------------------------------------------------------- epilogue
+      ok = wait_bounded(bar(ctl.unit_done), uit & 1, wc);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const bool live = q < p.N;
+      uint16_t* dst_row = reinterpret_cast<uint16_t*>(p.dq) + ((size_t)bh * p.N + q) * D + (D / 2) * h;
+#pragma unroll 1
+      for (int cc = 0; cc < D / 2; cc += 32) {
+        uint32_t av[32];
+        __syncwarp();
+        tmem_ld32(tmem + lane_off + kColDQ + (D / 2) * h + cc, av);
+        tmem_wait_ld();
+        reg_fence(av);
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          pk[e] = pack_bf16x2(__uint_as_float(av[2 * e]) * p.scale, __uint_as_float(av[2 * e + 1]) * p.scale);
+        if (live) {
+          uint4* dst = reinterpret_cast<uint4*>(dst_row + cc);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+        }
+      }
+      tc_fence_before();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 9) tmem_dealloc(tmem, C::kTmemCols);
+}
+
+// ============================================================================
+// Preprocessing: D_i = rowdot(dO_i, O_i) and L'_i = L_i * log2(e), padded to
+// Npad rows (L' = +inf, D = 0 past N so that padded queries get P = 0).  One
+// warp per row.
+// ============================================================================
+template <int D>
+__global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const uint16_t* __restrict__ o,
+                                                            const uint16_t* __restrict__ dO,
+                                                            const float* __restrict__ lse,
+                                                            float* __restrict__ lp, float* __restrict__ dd,
+                                                            int N, int Npad, long long rows_pad) {
+  const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows_pad) return;
+  const long long bh = row / Npad;
+  const int n = static_cast<int>(row - bh * Npad);
+  float acc = 0.0f;
+  if (n < N) {
+    const size_t base = ((size_t)bh * N + n) * D;
+    constexpr int V = D / 32;   // elements per lane (4 or 2)
+    const uint16_t* po = o + base + V * lane;
+    const uint16_t* pd = dO + base + V * lane;
+#pragma unroll
+    for (int e = 0; e < V; ++e)
+      acc = fmaf(__uint_as_float(static_cast<uint32_t>(po[e]) << 16),
+                 __uint_as_float(static_cast<uint32_t>(pd[e]) << 16), acc);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) {
+    dd[row] = acc;
+    lp[row] = n < N ? lse[(size_t)bh * N + n] * 1.4426950408889634f : __int_as_float(0x7f800000);
+  }
+}
+
+}  // namespace gb300

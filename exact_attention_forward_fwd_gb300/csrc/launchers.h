@@ -28,4 +28,13 @@ cudaError_t launch_fp8_prep(const void* x, void* x8, float* scales, const signed
 cudaError_t launch_splitkv_merge(const float* o_part, const float* lse_part, void* o, float* lse,
                                  int splits, int BH, int N, int D, cudaStream_t stream);
 
+// Attention backward: prep (D, scaled lse), dK/dV kernel, dQ kernel, in
+// order on `stream`.  lp, dd: [BH][Npad] f32 scratch.
+struct BwdParams;
+cudaError_t launch_attn_bwd(int d, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                            const CUtensorMap& dO, const BwdParams& p, const void* o,
+                            const void* dO_ptr, const float* lse, float* lp, float* dd, int sms,
+                            cudaStream_t stream);
+int status_attn_bwd(bool clear);
+
 }  // namespace gb300

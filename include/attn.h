@@ -180,6 +180,38 @@ ATTN_API int attn_fwd_fp8(const void* q8, const void* k8, const void* v8t, const
                  const float* k_scale, const float* v_scale, void* o, float* lse, int B, int H,
                  int N, int d, float scale, int causal, attn_stream_t stream);
 
+/* Attention backward: gradients of O = softmax(scale Q K^T [+mask]) V with
+ * respect to Q, K, V, given the incoming gradient dO and the forward's O and
+ * logsumexp ("4.3 FlashAttention 2 & 3", section "The backward pass:
+ * recompute, and the one identity that makes it tile-able"):
+ *     P = exp(scale Q K^T - L) (recomputed tile by tile, never stored),
+ *     D_i = rowdot(dO_i, O_i),  dV = P^T dO,  dP = dO V^T,  dS = P o (dP - D),
+ *     dQ = scale dS K,  dK = scale dS^T Q.
+ * With grouped KV heads, dK and dV of a KV head sum the contributions of the
+ * query heads that read it.  Deterministic: dK, dV are accumulated by the
+ * kernel that owns a key block, dQ by a second kernel that owns a query block
+ * (no atomic adds).  P and dS enter the tensor-core products rounded to bf16;
+ * accumulation is f32; outputs are rounded to bf16 (nearest even).
+ *   q, k, v, o, lse, B, H, H_kv, N, d, scale, causal, window : as attn_fwd_ex;
+ *            o and lse are that call's outputs (lse is required here).
+ *   dO     : bf16 [B, H, N, d], read only.
+ *   dq     : bf16 [B, H, N, d], written.   dk, dv : bf16 [B, H_kv, N, d], written.
+ *   workspace : caller-owned device scratch, 16-byte aligned, of at least
+ *            attn_bwd_workspace_bytes(B, H, N, d) bytes (overwritten; calls
+ *            sharing it must be ordered).
+ * Errors: as attn_fwd_ex; ATTN_ERR_INVALID_ARG for a NULL pointer (lse
+ * included) or a too small workspace; ATTN_ERR_ALIGNMENT for dO, dq, dk, dv,
+ * workspace not 16-byte aligned. */
+ATTN_API int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                      const void* dO, void* dq, void* dk, void* dv, int B, int H, int H_kv, int N,
+                      int d, float scale, int causal, int window, void* workspace,
+                      size_t workspace_bytes, attn_stream_t stream);
+
+/* Workspace bytes attn_bwd needs: two f32 arrays of B * H * Npad values (the
+ * scaled logsumexp and D, Npad = 128 * ceil(N / 128)), each rounded up to a
+ * multiple of 256 bytes; 0 for invalid arguments.  Host arithmetic. */
+ATTN_API size_t attn_bwd_workspace_bytes(int B, int H, int N, int d);
+
 /* attn_fwd with an explicit status word and wait limit, for tests of the
  * failure path.  dev_status: device int, set to ATTN_ERR_TIMEOUT by a kernel
  * whose wait ran out (the caller clears it first).  timeout_ns: wait limit.

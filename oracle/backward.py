@@ -80,3 +80,48 @@ def backward(q, k, v, dO, scale: float, causal: bool, window: int = 0):
 def row_dot(dO, O):
     """D_i = sum_t dO_it O_it: the page's form of D (used by the tests only)."""
     return (dO * O).sum(axis=-1)
+
+
+def backward_sampled(q, k, v, dO, scale: float, causal: bool, rows, keys, window: int = 0):
+    """The same definition restricted to some outputs of one (batch, head):
+    dQ for the listed query ``rows`` and dK, dV for the listed ``keys``.
+
+    Row i of dQ needs row i of P and dP; key j of dK, dV needs column j of P,
+    which needs every row's normaliser: the softmax is taken row by row over
+    all keys (in chunks of rows, so that no N x N array is formed)."""
+    N = k.shape[0]
+    rows = np.asarray(rows, dtype=np.int64)
+    keys = np.asarray(keys, dtype=np.int64)
+
+    def prob_rows(r):
+        S = scale * (q[r] @ k.T)
+        if causal:
+            j = np.arange(N)[None, :]
+            vis = j <= r[:, None]
+            if window > 0:
+                vis &= j > r[:, None] - window
+            S = np.where(vis, S, -np.inf)
+        m = S.max(axis=1, keepdims=True)
+        live = np.isfinite(m)
+        E = np.where(np.isfinite(S), np.exp(S - np.where(live, m, 0.0)), 0.0)
+        ell = E.sum(axis=1, keepdims=True)
+        return np.where(live, E / np.where(live, ell, 1.0), 0.0)
+
+    # dQ rows: full rows of P and dP.
+    P = prob_rows(rows)
+    dP = dO[rows] @ v.T
+    D = (P * dP).sum(axis=1)
+    dQ = scale * ((P * (dP - D[:, None])) @ k)
+    # dK, dV keys: the listed columns of P for all rows, plus every row's D.
+    dK = np.zeros((keys.size, q.shape[1]))
+    dV = np.zeros((keys.size, v.shape[1]))
+    for c0 in range(0, N, 512):
+        r = np.arange(c0, min(N, c0 + 512))
+        Pr = prob_rows(r)
+        dPr = dO[r] @ v.T
+        Dr = (Pr * dPr).sum(axis=1)
+        Pc = Pr[:, keys]
+        dSc = Pc * (dPr[:, keys] - Dr[:, None])
+        dV += Pc.T @ dO[r]
+        dK += scale * (dSc.T @ q[r])
+    return dQ, dK, dV

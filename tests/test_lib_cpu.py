@@ -155,3 +155,20 @@ def test_splitkv_validation_codes(L):
     assert f(nbytes=ga.splitkv_workspace_bytes(1, 2, 256, 128, 2) - 1) == ga.ATTN_ERR_INVALID_ARG
     assert f(ws=ctypes.c_void_p(A.value + 8)) == ga.ATTN_ERR_ALIGNMENT
     assert f(d=96) == ga.ATTN_ERR_UNSUPPORTED
+
+
+def test_bwd_workspace_and_validation(L):
+    Npad = lambda N: (N + 127) // 128 * 128
+    up = lambda x: (x + 255) // 256 * 256
+    for B, H, N, d in [(1, 2, 300, 64), (2, 16, 8192, 128), (1, 1, 1, 128)]:
+        assert ga.bwd_workspace_bytes(B, H, N, d) == 2 * up(B * H * Npad(N) * 4)
+    assert ga.bwd_workspace_bytes(1, 1, 1, 96) == 0
+    f = lambda lse=A, ws=A, nbytes=1 << 30, d=128, H_kv=2, causal=0, window=0: L.attn_bwd(
+        A, A, A, A, lse, A, A, A, A, 1, 2, H_kv, 256, d, 0.1, causal, window, ws, nbytes, None)
+    assert f(lse=None) == ga.ATTN_ERR_INVALID_ARG
+    assert f(ws=None) == ga.ATTN_ERR_INVALID_ARG
+    assert f(nbytes=ga.bwd_workspace_bytes(1, 2, 256, 128) - 1) == ga.ATTN_ERR_INVALID_ARG
+    assert f(H_kv=3) == ga.ATTN_ERR_INVALID_ARG
+    assert f(window=5) == ga.ATTN_ERR_INVALID_ARG
+    assert f(d=96) == ga.ATTN_ERR_UNSUPPORTED
+    assert f(ws=ctypes.c_void_p(A.value + 8)) == ga.ATTN_ERR_ALIGNMENT

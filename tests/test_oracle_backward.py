@@ -123,3 +123,16 @@ def test_causal_row_zero_has_zero_dQ_and_last_key_sees_only_last_row():
     np.testing.assert_allclose(dQ[0], 0.0, atol=1e-14)          # one visible key: P = 1
     P = ob.softmax_weights(q, k, scale, True)
     np.testing.assert_allclose(dV[-1], P[-1, -1] * dO[-1], rtol=1e-12)
+
+
+@pytest.mark.parametrize("causal,window", [(False, 0), (True, 0), (True, 9)])
+def test_sampled_outputs_equal_full_backward(causal, window):
+    N, d, scale = 700, 8, 0.4
+    q, k, v, dO = (_rand((N, d), s) for s in (61, 62, 63, 64))
+    dQ, dK, dV = ob.backward_head(q, k, v, dO, scale, causal, window)
+    rows = [0, 1, 127, 128, 511, 512, 699]
+    keys = [0, 5, 300, 698, 699]
+    sq, sk, sv = ob.backward_sampled(q, k, v, dO, scale, causal, rows, keys, window)
+    np.testing.assert_allclose(sq, dQ[rows], rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(sk, dK[keys], rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(sv, dV[keys], rtol=1e-10, atol=1e-12)
