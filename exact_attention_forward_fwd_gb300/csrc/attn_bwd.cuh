@@ -17,9 +17,12 @@
 //     (query block, key block) instead of 5).
 //
 // Blackwell mapping (this file's own design), both kernels one persistent CTA
-// per SM, 320 threads: warps 0-7 element-wise work (warp w owns TMEM lane
-// quarter w & 3 and half w >> 2 of the tile's columns), warp 8 TMA, warp 9
-// TMEM allocation and every tcgen05.mma from one thread.
+// per SM, 576 threads: warps 0-15 element-wise work (warp w owns TMEM lane
+// quarter w & 3 and the 32 tile columns [32(w >> 2), +32)), warp 16 TMA, warp
+// 17 TMEM allocation and every tcgen05.mma from one thread.  Sixteen
+// element-wise warps (four per SM sub-partition) hide the latency of the TMEM
+// loads; the per-query L and D of the dK/dV kernel arrive in shared memory by
+// bulk copy with each Q tile.
 //   dK/dV kernel (keys on the TMEM lanes): S^T = K Q^T and dP^T = V dO^T (SS);
 //     P^T (bf16) over S^T, dS^T (bf16) over dP^T; dV += P^T dO and
 //     dK += dS^T Q (TS, P^T / dS^T straight from TMEM, Q and dO as MN-major
@@ -60,14 +63,25 @@ struct BCfg {
   static_assert(D == 64 || D == 128, "head dim 64 or 128");
   static constexpr int kTile = 128 * D * 2;                 // 128 rows x D bf16
   static constexpr int kSlabs = D / 64;                     // 128-byte column slabs
-  static constexpr int kStages = (D == 128) ? 5 : 10;       // ring of tiles
-  static constexpr int kSmemBytes = (2 + kStages) * kTile + 1024;
+  static constexpr int kStages = (D == 128) ? 4 : 8;        // ring of tiles
+  static constexpr int kStatBytes = 2 * 128 * 4;            // L' and D of one query block
+  static constexpr int kSmemBytes = (2 + kStages) * kTile + kStages * kStatBytes + 1024;
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr int kThreads = 320;
+  static constexpr int kEW = 16;                            // element-wise warps
+  static constexpr int kThreads = (kEW + 2) * 32;
   static constexpr int kSSteps = D / 16;                    // K = D for S, dP
   static constexpr uint32_t kIdescSS = make_idesc(128, 128, 1, 1, false, false);
   static constexpr uint32_t kIdescTS = make_idesc(128, D, 1, 1, false, true);
 };
+
+// Bulk copy (no tensor map) of `bytes` (multiple of 16, both addresses 16-byte
+// aligned) into this CTA's shared memory, completing on an mbarrier.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
 
 struct BwdCtl {
   uint64_t full[16];       // ring slot loaded
@@ -75,8 +89,8 @@ struct BwdCtl {
   uint64_t fix_full;       // the unit's fixed tiles (K, V or Q, dO) loaded
   uint64_t fix_empty;      // ... free again
   uint64_t s_full;         // S and dP of a block computed
-  uint64_t p_ready;        // dK/dV: P^T written; dQ: dS written (8 warp arrivals)
-  uint64_t ds_ready;       // dK/dV: dS^T written (8 warp arrivals)
+  uint64_t p_ready;        // dK/dV: P^T written; dQ: dS written (16 warp arrivals)
+  uint64_t ds_ready;       // dK/dV: dS^T written (16 warp arrivals)
   uint64_t unit_done;      // the unit's accumulators final
   uint64_t drain;
   uint32_t tmem_base;
@@ -105,7 +119,7 @@ __device__ __forceinline__ bool bwd_visible(int k, int q, const BwdParams& p) {
 // dK, dV: one unit = (batch * KV head, 128-key block j).
 // ============================================================================
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(576, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                          const BwdParams p) {
@@ -117,6 +131,9 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t sK = smem_addr(smem);
   const uint32_t sV = sK + C::kTile;
   const uint32_t sRing = sV + C::kTile;     // Q_i / dO_i tiles, alternating
+  // L' and D of the query block of the Q item in ring slot s: 128 + 128 floats
+  const uint32_t sStat = sRing + C::kStages * C::kTile;
+  const float* stat = reinterpret_cast<const float*>(smem + (2 + C::kStages) * C::kTile);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   auto bar = [&](uint64_t& b) { return smem_addr(&b); };
@@ -129,15 +146,15 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(bar(ctl.fix_full), 1);
     mbar_init(bar(ctl.fix_empty), 1);
     mbar_init(bar(ctl.s_full), 1);
-    mbar_init(bar(ctl.p_ready), 8);
-    mbar_init(bar(ctl.ds_ready), 8);
+    mbar_init(bar(ctl.p_ready), C::kEW);
+    mbar_init(bar(ctl.ds_ready), C::kEW);
     mbar_init(bar(ctl.unit_done), 1);
     mbar_init(bar(ctl.drain), 1);
     ctl.abort_flag = 0;
     fence_mbarrier_init();
     fence_proxy_async_smem();
   }
-  if (warp == 9) {
+  if (warp == C::kEW + 1) {
     tmem_alloc(smem_addr(&ctl.tmem_base), C::kTmemCols);
     tmem_relinquish();
   }
@@ -159,7 +176,7 @@ __global__ void __launch_bounds__(320, 1)
     }
   };
 
-  if (warp == 8) {
+  if (warp == C::kEW) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       prefetch_tensormap(&tmQ);
@@ -186,13 +203,18 @@ __global__ void __launch_bounds__(320, 1)
         for (int t = 0; t < p.group * nI && ok; ++t) {
           const int hh = t / nI, i = i_lo + (t - hh * nI);
           const int bh = b * p.H + g * p.group + hh;
-          for (int w2 = 0; w2 < 2 && ok; ++w2, ++item) {   // Q_i, then dO_i
+          for (int w2 = 0; w2 < 2 && ok; ++w2, ++item) {   // Q_i (+ L', D), then dO_i
             const uint32_t slot = item % C::kStages;
             if (!(ok = wait_bounded(bar(ctl.empty[slot]), ((item / C::kStages) & 1) ^ 1, wc))) break;
-            mbar_arrive_expect_tx(bar(ctl.full[slot]), C::kTile);
+            mbar_arrive_expect_tx(bar(ctl.full[slot]), C::kTile + (w2 == 0 ? C::kStatBytes : 0));
             for (int s = 0; s < C::kSlabs; ++s)
               tma_load_3d_hint(sRing + slot * C::kTile + s * 16384, w2 == 0 ? &tmQ : &tmdO,
                                bar(ctl.full[slot]), s * 64, i * 128, bh, pol_ring);
+            if (w2 == 0) {
+              const size_t off = (size_t)bh * p.Npad + (size_t)i * 128;
+              bulk_load(sStat + slot * C::kStatBytes, p.lp + off, 512, bar(ctl.full[slot]));
+              bulk_load(sStat + slot * C::kStatBytes + 512, p.dd + off, 512, bar(ctl.full[slot]));
+            }
           }
         }
       }
@@ -204,7 +226,7 @@ __global__ void __launch_bounds__(320, 1)
       }
       if (uit > 0) wait_bounded(bar(ctl.fix_full), (uit - 1) & 1, wc, false);
     }
-  } else if (warp == 9) {
+  } else if (warp == C::kEW + 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       uint32_t item = 0, uit = 0, gblk = 0;
@@ -221,12 +243,12 @@ __global__ void __launch_bounds__(320, 1)
                      make_smem_desc(b0 + off, 16, 1024, kSwizzle128B), C::kIdescSS, k > 0);
         }
       };
-      // TS product: A = 128 x 128 bf16 in TMEM (queries [0,64) at a_col,
-      // [64,128) at a_col + 64), B = a [queries x D] tile as MN-major operand.
+      // TS product: A = 128 x 128 bf16 in TMEM, queries [32h, 32h+32) at
+      // columns a_col + 32h + [0,16); B = a [queries x D] tile as MN-major operand.
       auto ts = [&](uint32_t d_col, uint32_t a_col, uint32_t b0, bool acc) {
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const uint32_t a = tmem + a_col + (k >> 2) * 64 + (k & 3) * 8;
+          const uint32_t a = tmem + a_col + (k >> 1) * 32 + (k & 1) * 8;
           mma_f16_ts(tmem + d_col, a, make_smem_desc(b0 + k * 2048, 16384, 1024, kSwizzle128B),
                      C::kIdescTS, (acc || k > 0) ? 1u : 0u);
         }
@@ -284,11 +306,11 @@ __global__ void __launch_bounds__(320, 1)
   } else {
     // ------------------------------------------------------------ element-wise
     const int qd = warp & 3;             // TMEM lane quarter: keys 32qd .. 32qd+31
-    const int h = warp >> 2;             // queries [64h, 64h+64) of each block
+    const int h = warp >> 2;             // queries [32h, 32h+32) of each block
     const int r = qd * 32 + lane;        // key row within the block
     const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
     const float cl = p.scale_log2;
-    uint32_t uit = 0, gblk = 0;
+    uint32_t uit = 0, gblk = 0, item = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uit) {
       int bhk, j;
@@ -296,73 +318,72 @@ __global__ void __launch_bounds__(320, 1)
       int i_lo, i_hi;
       bwd_qrange(j, p, i_lo, i_hi);
       const int nI = i_hi - i_lo + 1;
-      const int b = bhk / p.Hk, g = bhk - (bhk / p.Hk) * p.Hk;
       const int key = j * 128 + r;
-      for (int t = 0; t < p.group * nI; ++t, ++gblk) {
-        const int hh = t / nI, i = i_lo + (t - hh * nI);
-        const int bh = b * p.H + g * p.group + hh;
-        const int q0 = i * 128 + 64 * h;   // first query of this thread's columns
+      for (int t = 0; t < p.group * nI; ++t, ++gblk, item += 2) {
+        const int i = i_lo + (t - (t / nI) * nI);
+        const int q0 = i * 128 + 32 * h;   // first query of this thread's columns
         // Mask needed unless every (key, query) of the block is visible.
         const bool full_vis = (!p.causal || j * 128 + 127 <= i * 128) &&
                               (p.window <= 0 || j * 128 > i * 128 + 127 - p.window);
+        // L' and D of this block's queries, staged with the Q tile (item's slot).
+        const float4* Ls4 = reinterpret_cast<const float4*>(stat + (item % C::kStages) * (C::kStatBytes / 4) + 32 * h);
+        const float4* Ds4 = Ls4 + 32;   // D follows L' (128 floats later)
         ok = wait_bounded(bar(ctl.s_full), gblk & 1, wc);
+        // The Q item's slot (with L', D) landed; it is not refilled before this
+        // block's dS^T is signalled, so the phase test is unambiguous.
+        if (ok) ok = wait_bounded(bar(ctl.full[item % C::kStages]), (item / C::kStages) & 1, wc);
         ok = __all_sync(0xffffffffu, ok);
-        ok = bar_and(1, 256, ok);
+        ok = bar_and(1, 32 * C::kEW, ok);
         if (!ok) break;
         tc_fence_after();
-        const float4* lq = reinterpret_cast<const float4*>(p.lp + (size_t)bh * p.Npad + q0);
-        const float4* dq4 = reinterpret_cast<const float4*>(p.dd + (size_t)bh * p.Npad + q0);
-        // ---- phase A: P^T = exp2(S^T * c - L') for this thread's 64 queries
-        float pr[64];
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
+        // ---- phase A: P^T = exp2(S^T * c - L') for this thread's 32 queries
+        float pr[32];
+        {
           uint32_t sv[32];
-          tmem_ld32(tmem + lane_off + 64 * h + 32 * c, sv);
+          tmem_ld32(tmem + lane_off + 32 * h, sv);
           tmem_wait_ld();
           reg_fence(sv);
           uint32_t pk[16];
 #pragma unroll
           for (int v4 = 0; v4 < 8; ++v4) {
-            const float4 L = __ldg(lq + 8 * c + v4);
-            const float Ls[4] = {L.x, L.y, L.z, L.w};
+            const float4 L = Ls4[v4];
+            const float Lv[4] = {L.x, L.y, L.z, L.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const int col = 32 * c + 4 * v4 + e;
-              float pv = ex2_approx(fmaf(__uint_as_float(sv[4 * v4 + e]), cl, -Ls[e]));
+              const int col = 4 * v4 + e;
+              float pv = ex2_approx(fmaf(__uint_as_float(sv[col]), cl, -Lv[e]));
               if (!full_vis && !bwd_visible(key, q0 + col, p)) pv = 0.0f;
               pr[col] = pv;
             }
           }
 #pragma unroll
-          for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(pr[32 * c + 2 * e], pr[32 * c + 2 * e + 1]);
-          // P^T of queries [64h + 32c, +32) -> columns [64h + 16c, +16): inside the
-          // S^T columns this thread has already read.
-          tmem_st16(tmem + lane_off + 64 * h + 16 * c, pk);
+          for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(pr[2 * e], pr[2 * e + 1]);
+          // P^T of queries [32h, +32) -> columns [32h, 32h+16): inside the S^T
+          // columns this warp has already read.
+          tmem_st16(tmem + lane_off + 32 * h, pk);
         }
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(ctl.p_ready));
         // ---- phase B: dS^T = P^T o (dP^T - D)
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
+        {
           uint32_t dv[32];
-          tmem_ld32(tmem + lane_off + 128 + 64 * h + 32 * c, dv);
+          tmem_ld32(tmem + lane_off + 128 + 32 * h, dv);
           tmem_wait_ld();
           reg_fence(dv);
           uint32_t pk[16];
 #pragma unroll
           for (int v4 = 0; v4 < 8; ++v4) {
-            const float4 Dv = __ldg(dq4 + 8 * c + v4);
-            const float Ds[4] = {Dv.x, Dv.y, Dv.z, Dv.w};
+            const float4 Dv = Ds4[v4];
+            const float Dd[4] = {Dv.x, Dv.y, Dv.z, Dv.w};
             float ds[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              ds[e] = pr[32 * c + 4 * v4 + e] * (__uint_as_float(dv[4 * v4 + e]) - Ds[e]);
+            for (int e = 0; e < 4; ++e) ds[e] = pr[4 * v4 + e] * (__uint_as_float(dv[4 * v4 + e]) - Dd[e]);
             pk[2 * v4] = pack_bf16x2(ds[0], ds[1]);
             pk[2 * v4 + 1] = pack_bf16x2(ds[2], ds[3]);
           }
-          tmem_st16(tmem + lane_off + 128 + 64 * h + 16 * c, pk);
+          tmem_st16(tmem + lane_off + 128 + 32 * h, pk);
         }
         tmem_wait_st();
         tc_fence_before();
@@ -376,27 +397,36 @@ __global__ void __launch_bounds__(320, 1)
       if (!ok) break;
       tc_fence_after();
       const bool live = key < p.N;
-      const size_t orow = ((size_t)bhk * p.N + key) * D + (D / 2) * h;
+      constexpr int kW = D / 4;   // output columns of this thread: [kW h, kW h + kW)
+      const size_t orow = ((size_t)bhk * p.N + key) * D + kW * h;
 #pragma unroll 1
       for (int which = 0; which < 2; ++which) {   // dV, then dK (times scale)
         const float mul = which == 0 ? 1.0f : p.scale;
         uint16_t* dst_row = reinterpret_cast<uint16_t*>(which == 0 ? p.dv : p.dk) + orow;
-#pragma unroll 1
-        for (int cc = 0; cc < D / 2; cc += 32) {
+        const uint32_t src = tmem + lane_off + 256 + which * D + kW * h;
+        uint32_t pk[kW / 2];
+        __syncwarp();
+        if (kW == 32) {
           uint32_t av[32];
-          __syncwarp();
-          tmem_ld32(tmem + lane_off + 256 + which * D + (D / 2) * h + cc, av);
+          tmem_ld32(src, av);
           tmem_wait_ld();
           reg_fence(av);
-          uint32_t pk[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
+          for (int e = 0; e < kW / 2; ++e)
             pk[e] = pack_bf16x2(__uint_as_float(av[2 * e]) * mul, __uint_as_float(av[2 * e + 1]) * mul);
-          if (live) {
-            uint4* dst = reinterpret_cast<uint4*>(dst_row + cc);
+        } else {
+          uint32_t av[16];
+          tmem_ld16(src, av);
+          tmem_wait_ld();
+          reg_fence(av);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
-          }
+          for (int e = 0; e < kW / 2; ++e)
+            pk[e] = pack_bf16x2(__uint_as_float(av[2 * e]) * mul, __uint_as_float(av[2 * e + 1]) * mul);
+        }
+        if (live) {
+          uint4* dst = reinterpret_cast<uint4*>(dst_row);
+#pragma unroll
+          for (int e = 0; e < kW / 8; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
         }
       }
       tc_fence_before();   // accumulators read: the next unit's first products may overwrite them
@@ -406,14 +436,14 @@ __global__ void __launch_bounds__(320, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 9) tmem_dealloc(tmem, C::kTmemCols);
+  if (warp == C::kEW + 1) tmem_dealloc(tmem, C::kTmemCols);
 }
 
 // ============================================================================
 // dQ: one unit = (batch * query head, 128-query block i).
 // ============================================================================
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(576, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                        const BwdParams p) {
@@ -438,15 +468,15 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(bar(ctl.fix_full), 1);
     mbar_init(bar(ctl.fix_empty), 1);
     mbar_init(bar(ctl.s_full), 1);
-    mbar_init(bar(ctl.p_ready), 8);
-    mbar_init(bar(ctl.ds_ready), 8);
+    mbar_init(bar(ctl.p_ready), C::kEW);
+    mbar_init(bar(ctl.ds_ready), C::kEW);
     mbar_init(bar(ctl.unit_done), 1);
     mbar_init(bar(ctl.drain), 1);
     ctl.abort_flag = 0;
     fence_mbarrier_init();
     fence_proxy_async_smem();
   }
-  if (warp == 9) {
+  if (warp == C::kEW + 1) {
     tmem_alloc(smem_addr(&ctl.tmem_base), C::kTmemCols);
     tmem_relinquish();
   }
@@ -473,7 +503,7 @@ __global__ void __launch_bounds__(320, 1)
   };
   auto sbuf = [&](uint32_t gg) { return (gg & 1) ? kColS1 : 0u; };
 
-  if (warp == 8) {
+  if (warp == C::kEW) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       prefetch_tensormap(&tmQ);
@@ -514,7 +544,7 @@ __global__ void __launch_bounds__(320, 1)
       }
       if (uit > 0) wait_bounded(bar(ctl.fix_full), (uit - 1) & 1, wc, false);
     }
-  } else if (warp == 9) {
+  } else if (warp == C::kEW + 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       uint32_t item = 0, uit = 0, gblk = 0;
@@ -572,7 +602,7 @@ __global__ void __launch_bounds__(320, 1)
           const uint32_t kb = slot_addr(ik);
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
-            const uint32_t a = tmem + a_col + (k >> 2) * 64 + (k & 3) * 8;
+            const uint32_t a = tmem + a_col + (k >> 1) * 32 + (k & 1) * 8;
             mma_f16_ts(tmem + kColDQ, a, make_smem_desc(kb + k * 2048, 16384, 1024, kSwizzle128B),
                        C::kIdescTS, (jj > 0 || k > 0) ? 1u : 0u);
           }
@@ -587,7 +617,7 @@ __global__ void __launch_bounds__(320, 1)
   } else {
     // ------------------------------------------------------------ element-wise
     const int qd = warp & 3;             // TMEM lane quarter: queries 32qd .. 32qd+31
-    const int h = warp >> 2;             // keys [64h, 64h+64) of each block
+    const int h = warp >> 2;             // keys [32h, 32h+32) of each block
     const int r = qd * 32 + lane;        // query row within the block
     const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
     const float cl = p.scale_log2;
@@ -602,38 +632,36 @@ __global__ void __launch_bounds__(320, 1)
       const float Lq = __ldg(p.lp + (size_t)bh * p.Npad + q);   // +inf past N: P = 0
       const float Dq = __ldg(p.dd + (size_t)bh * p.Npad + q);
       for (int jj = j_lo; jj <= j_hi; ++jj, ++gblk) {
+        const int k0 = jj * 128 + 32 * h;   // first key of this thread's columns
         const bool full_vis = (jj * 128 + 127 < p.N) && (!p.causal || jj * 128 + 127 <= i * 128) &&
                               (p.window <= 0 || jj * 128 > i * 128 + 127 - p.window);
         ok = wait_bounded(bar(ctl.s_full), gblk & 1, wc);
         ok = __all_sync(0xffffffffu, ok);
-        ok = bar_and(1, 256, ok);
+        ok = bar_and(1, 32 * C::kEW, ok);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t scol = sbuf(gblk) + 64 * h;
+        const uint32_t scol = sbuf(gblk) + 32 * h;
+        uint32_t sv[32], dv[32];
+        tmem_ld32(tmem + lane_off + scol, sv);
+        tmem_ld32(tmem + lane_off + kColDP + 32 * h, dv);
+        tmem_wait_ld();
+        reg_fence(sv);
+        reg_fence(dv);
+        uint32_t pk[16];
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t sv[32], dv[32];
-          tmem_ld32(tmem + lane_off + scol + 32 * c, sv);
-          tmem_ld32(tmem + lane_off + kColDP + 64 * h + 32 * c, dv);
-          tmem_wait_ld();
-          reg_fence(sv);
-          reg_fence(dv);
-          uint32_t pk[16];
+        for (int e = 0; e < 16; ++e) {
+          float ds2[2];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            float ds2[2];
-#pragma unroll
-            for (int z = 0; z < 2; ++z) {
-              const int col = 2 * e + z;
-              float pv = ex2_approx(fmaf(__uint_as_float(sv[col]), cl, -Lq));
-              if (!full_vis && !bwd_visible(jj * 128 + 64 * h + 32 * c + col, q, p)) pv = 0.0f;
-              ds2[z] = pv * (__uint_as_float(dv[col]) - Dq);
-            }
-            pk[e] = pack_bf16x2(ds2[0], ds2[1]);
+          for (int z = 0; z < 2; ++z) {
+            const int col = 2 * e + z;
+            float pv = ex2_approx(fmaf(__uint_as_float(sv[col]), cl, -Lq));
+            if (!full_vis && !bwd_visible(k0 + col, q, p)) pv = 0.0f;
+            ds2[z] = pv * (__uint_as_float(dv[col]) - Dq);
           }
-          // dS of keys [64h + 32c, +32) -> columns [64h + 16c, +16) of this S buffer
-          tmem_st16(tmem + lane_off + scol + 16 * c, pk);
+          pk[e] = pack_bf16x2(ds2[0], ds2[1]);
         }
+        // dS of keys [32h, +32) -> columns [32h, 32h+16) of this S buffer
+        tmem_st16(tmem + lane_off + scol, pk);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -646,23 +674,32 @@ __global__ void __launch_bounds__(320, 1)
       if (!ok) break;
       tc_fence_after();
       const bool live = q < p.N;
-      uint16_t* dst_row = reinterpret_cast<uint16_t*>(p.dq) + ((size_t)bh * p.N + q) * D + (D / 2) * h;
-#pragma unroll 1
-      for (int cc = 0; cc < D / 2; cc += 32) {
+      constexpr int kW = D / 4;   // output columns of this thread: [kW h, kW h + kW)
+      uint16_t* dst_row = reinterpret_cast<uint16_t*>(p.dq) + ((size_t)bh * p.N + q) * D + kW * h;
+      const uint32_t src = tmem + lane_off + kColDQ + kW * h;
+      uint32_t pk[kW / 2];
+      __syncwarp();
+      if (kW == 32) {
         uint32_t av[32];
-        __syncwarp();
-        tmem_ld32(tmem + lane_off + kColDQ + (D / 2) * h + cc, av);
+        tmem_ld32(src, av);
         tmem_wait_ld();
         reg_fence(av);
-        uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e)
+        for (int e = 0; e < kW / 2; ++e)
           pk[e] = pack_bf16x2(__uint_as_float(av[2 * e]) * p.scale, __uint_as_float(av[2 * e + 1]) * p.scale);
-        if (live) {
-          uint4* dst = reinterpret_cast<uint4*>(dst_row + cc);
+      } else {
+        uint32_t av[16];
+        tmem_ld16(src, av);
+        tmem_wait_ld();
+        reg_fence(av);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
-        }
+        for (int e = 0; e < kW / 2; ++e)
+          pk[e] = pack_bf16x2(__uint_as_float(av[2 * e]) * p.scale, __uint_as_float(av[2 * e + 1]) * p.scale);
+      }
+      if (live) {
+        uint4* dst = reinterpret_cast<uint4*>(dst_row);
+#pragma unroll
+        for (int e = 0; e < kW / 8; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
       }
       tc_fence_before();
     }
@@ -671,7 +708,7 @@ __global__ void __launch_bounds__(320, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 9) tmem_dealloc(tmem, C::kTmemCols);
+  if (warp == C::kEW + 1) tmem_dealloc(tmem, C::kTmemCols);
 }
 
 // ============================================================================
