@@ -23,7 +23,7 @@ cudaError_t run_bwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMa
   auto kdq = attn_bwd_dq_kernel<D>;
   if ((e = cudaFuncSetAttribute(kdkdv, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes)) !=
           cudaSuccess ||
-      (e = cudaFuncSetAttribute(kdq, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes)) !=
+      (e = cudaFuncSetAttribute(kdq, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytesDQ)) !=
           cudaSuccess)
     return e;
   BwdParams p1 = base;
@@ -34,7 +34,7 @@ cudaError_t run_bwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMa
   BwdParams p2 = base;
   p2.num_units = base.BH * base.nb;
   const int g2 = p2.num_units < sms ? p2.num_units : sms;
-  kdq<<<g2, C::kThreads, C::kSmemBytes, stream>>>(q, k, v, dO, p2);
+  kdq<<<g2, C::kThreads, C::kSmemBytesDQ, stream>>>(q, k, v, dO, p2);
   return cudaGetLastError();
 }
 

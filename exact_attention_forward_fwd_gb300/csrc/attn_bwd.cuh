@@ -63,9 +63,14 @@ struct BCfg {
   static_assert(D == 64 || D == 128, "head dim 64 or 128");
   static constexpr int kTile = 128 * D * 2;                 // 128 rows x D bf16
   static constexpr int kSlabs = D / 64;                     // 128-byte column slabs
-  static constexpr int kStages = (D == 128) ? 4 : 8;        // ring of tiles
+  // Ring of tiles: dK/dV kernel Q/dO tiles (+ L', D of each Q tile's block);
+  // dQ kernel K/V tiles (5 slots at D = 128: K_{j+2} can load while K_j, V_j+1,
+  // K_j+1 are in use).
+  static constexpr int kStages = (D == 128) ? 4 : 8;
+  static constexpr int kStagesDQ = (D == 128) ? 5 : 10;
   static constexpr int kStatBytes = 2 * 128 * 4;            // L' and D of one query block
   static constexpr int kSmemBytes = (2 + kStages) * kTile + kStages * kStatBytes + 1024;
+  static constexpr int kSmemBytesDQ = (2 + kStagesDQ) * kTile + 1024;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr int kEW = 16;                            // element-wise warps
   static constexpr int kThreads = (kEW + 2) * 32;
@@ -343,18 +348,26 @@ __global__ void __launch_bounds__(576, 1)
           tmem_ld32(tmem + lane_off + 32 * h, sv);
           tmem_wait_ld();
           reg_fence(sv);
+          if (!full_vis) {
+            // Diagonal / window-edge block: 2^-inf = 0 for the invisible scores.
+#pragma unroll
+            for (int col = 0; col < 32; ++col)
+              if (!bwd_visible(key, q0 + col, p)) sv[col] = 0xff800000u;
+          }
+          const uint64_t c2 = f32x2_pack(cl, cl);
           uint32_t pk[16];
 #pragma unroll
           for (int v4 = 0; v4 < 8; ++v4) {
             const float4 L = Ls4[v4];
-            const float Lv[4] = {L.x, L.y, L.z, L.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int col = 4 * v4 + e;
-              float pv = ex2_approx(fmaf(__uint_as_float(sv[col]), cl, -Lv[e]));
-              if (!full_vis && !bwd_visible(key, q0 + col, p)) pv = 0.0f;
-              pr[col] = pv;
-            }
+            float a0, a1, a2, a3;
+            f32x2_unpack(f32x2_fma(f32x2_pack(__uint_as_float(sv[4 * v4]), __uint_as_float(sv[4 * v4 + 1])), c2,
+                                   f32x2_pack(-L.x, -L.y)), a0, a1);
+            f32x2_unpack(f32x2_fma(f32x2_pack(__uint_as_float(sv[4 * v4 + 2]), __uint_as_float(sv[4 * v4 + 3])), c2,
+                                   f32x2_pack(-L.z, -L.w)), a2, a3);
+            pr[4 * v4] = ex2_approx(a0);
+            pr[4 * v4 + 1] = ex2_approx(a1);
+            pr[4 * v4 + 2] = ex2_approx(a2);
+            pr[4 * v4 + 3] = ex2_approx(a3);
           }
 #pragma unroll
           for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(pr[2 * e], pr[2 * e + 1]);
@@ -461,7 +474,7 @@ __global__ void __launch_bounds__(576, 1)
   constexpr uint32_t kColDP = 128, kColDQ = 256, kColS1 = 384;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::kStages; ++s) {
+    for (int s = 0; s < C::kStagesDQ; ++s) {
       mbar_init(bar(ctl.full[s]), 1);
       mbar_init(bar(ctl.empty[s]), 1);
     }
@@ -528,8 +541,8 @@ __global__ void __launch_bounds__(576, 1)
         }
         for (int jj = j_lo; jj <= j_hi && ok; ++jj) {
           for (int w2 = 0; w2 < 2 && ok; ++w2, ++item) {   // K_j, then V_j
-            const uint32_t slot = item % C::kStages;
-            if (!(ok = wait_bounded(bar(ctl.empty[slot]), ((item / C::kStages) & 1) ^ 1, wc))) break;
+            const uint32_t slot = item % C::kStagesDQ;
+            if (!(ok = wait_bounded(bar(ctl.empty[slot]), ((item / C::kStagesDQ) & 1) ^ 1, wc))) break;
             mbar_arrive_expect_tx(bar(ctl.full[slot]), C::kTile);
             for (int s = 0; s < C::kSlabs; ++s)
               tma_load_3d_hint(sRing + slot * C::kTile + s * 16384, w2 == 0 ? &tmK : &tmV,
@@ -538,9 +551,9 @@ __global__ void __launch_bounds__(576, 1)
         }
       }
       const uint32_t issued = item;
-      for (uint32_t s = 0; s < (uint32_t)C::kStages && s < issued; ++s) {
-        const uint32_t last = s + ((issued - 1 - s) / C::kStages) * C::kStages;
-        wait_bounded(bar(ctl.full[s]), (last / C::kStages) & 1, wc, false);
+      for (uint32_t s = 0; s < (uint32_t)C::kStagesDQ && s < issued; ++s) {
+        const uint32_t last = s + ((issued - 1 - s) / C::kStagesDQ) * C::kStagesDQ;
+        wait_bounded(bar(ctl.full[s]), (last / C::kStagesDQ) & 1, wc, false);
       }
       if (uit > 0) wait_bounded(bar(ctl.fix_full), (uit - 1) & 1, wc, false);
     }
@@ -550,7 +563,7 @@ __global__ void __launch_bounds__(576, 1)
       uint32_t item = 0, uit = 0, gblk = 0;
       bool ok = true;
       auto wait_slot = [&](uint32_t it) {
-        return wait_bounded(bar(ctl.full[it % C::kStages]), (it / C::kStages) & 1, wc);
+        return wait_bounded(bar(ctl.full[it % C::kStagesDQ]), (it / C::kStagesDQ) & 1, wc);
       };
       auto ss = [&](uint32_t d_col, uint32_t a0, uint32_t b0) {
 #pragma unroll
@@ -560,7 +573,7 @@ __global__ void __launch_bounds__(576, 1)
                      make_smem_desc(b0 + off, 16, 1024, kSwizzle128B), C::kIdescSS, k > 0);
         }
       };
-      auto slot_addr = [&](uint32_t it) { return sRing + (it % C::kStages) * C::kTile; };
+      auto slot_addr = [&](uint32_t it) { return sRing + (it % C::kStagesDQ) * C::kTile; };
       for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uit) {
         int bh, i;
         unit(u, bh, i);
@@ -577,7 +590,7 @@ __global__ void __launch_bounds__(576, 1)
         ss(sbuf(g0), sQ, slot_addr(base));
         ss(kColDP, sdO, slot_addr(base + 1));
         mma_commit(bar(ctl.s_full));
-        mma_commit(bar(ctl.empty[(base + 1) % C::kStages]));   // V_0 done
+        mma_commit(bar(ctl.empty[(base + 1) % C::kStagesDQ]));   // V_0 done
         for (int jj = 0; jj < J && ok; ++jj, ++gblk) {
           const uint32_t ik = base + 2 * jj;
           const bool more = jj + 1 < J;
@@ -595,7 +608,7 @@ __global__ void __launch_bounds__(576, 1)
             tc_fence_after();
             ss(kColDP, sdO, slot_addr(ik + 3));
             mma_commit(bar(ctl.s_full));
-            mma_commit(bar(ctl.empty[(ik + 3) % C::kStages]));   // V_{jj+1} done
+            mma_commit(bar(ctl.empty[(ik + 3) % C::kStagesDQ]));   // V_{jj+1} done
           }
           // dQ += dS K_j (K_j as MN-major B)
           const uint32_t a_col = sbuf(gblk);
@@ -606,7 +619,7 @@ __global__ void __launch_bounds__(576, 1)
             mma_f16_ts(tmem + kColDQ, a, make_smem_desc(kb + k * 2048, 16384, 1024, kSwizzle128B),
                        C::kIdescTS, (jj > 0 || k > 0) ? 1u : 0u);
           }
-          mma_commit(bar(ctl.empty[ik % C::kStages]));   // K_j done
+          mma_commit(bar(ctl.empty[ik % C::kStagesDQ]));   // K_j done
         }
         mma_commit(bar(ctl.unit_done));
         mma_commit(bar(ctl.fix_empty));
@@ -647,18 +660,25 @@ __global__ void __launch_bounds__(576, 1)
         tmem_wait_ld();
         reg_fence(sv);
         reg_fence(dv);
+        if (!full_vis) {
+          // Diagonal / window-edge / ragged block: zero the invisible scores'
+          // probabilities through their exponent (2^-inf = 0).
+#pragma unroll
+          for (int col = 0; col < 32; ++col)
+            if (!bwd_visible(k0 + col, q, p)) sv[col] = 0xff800000u;
+        }
+        const uint64_t c2 = f32x2_pack(cl, cl);
+        const uint64_t nl2 = f32x2_pack(-Lq, -Lq);
+        const uint64_t nd2 = f32x2_pack(-Dq, -Dq);
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          float ds2[2];
-#pragma unroll
-          for (int z = 0; z < 2; ++z) {
-            const int col = 2 * e + z;
-            float pv = ex2_approx(fmaf(__uint_as_float(sv[col]), cl, -Lq));
-            if (!full_vis && !bwd_visible(k0 + col, q, p)) pv = 0.0f;
-            ds2[z] = pv * (__uint_as_float(dv[col]) - Dq);
-          }
-          pk[e] = pack_bf16x2(ds2[0], ds2[1]);
+          float a0, a1, g0, g1;
+          f32x2_unpack(f32x2_fma(f32x2_pack(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), c2, nl2),
+                       a0, a1);
+          f32x2_unpack(f32x2_add(f32x2_pack(__uint_as_float(dv[2 * e]), __uint_as_float(dv[2 * e + 1])), nd2),
+                       g0, g1);
+          pk[e] = pack_bf16x2(ex2_approx(a0) * g0, ex2_approx(a1) * g1);
         }
         // dS of keys [32h, +32) -> columns [32h, 32h+16) of this S buffer
         tmem_st16(tmem + lane_off + scol, pk);
