@@ -487,21 +487,27 @@ __global__ void __launch_bounds__(320, 1)
         const float m_use = (m_ref == NEG_INF) ? 0.0f : m_ref;
         __syncwarp();   // tcgen05.st is warp-collective: reconverge after the mask branch
         if (FP8) {
-          float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+          // p' = p * v_fold = 2^(s c - (m - log2 v_fold)): V's block scale rides in
+          // the exponent, and the block's sum of p is sum(p') / v_fold.
+          const float m_f = m_use - __log2f(v_fold);
+          const uint64_t c2 = f32x2_pack(cj, cj);
+          const uint64_t nm2 = f32x2_pack(-m_f, -m_f);
+          uint64_t s01 = 0, s23 = 0;   // (0.f, 0.f)
           uint32_t pk[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const float p0 = ex2_approx(fmaf(x[4 * i], cj, -m_use));
-            const float p1 = ex2_approx(fmaf(x[4 * i + 1], cj, -m_use));
-            const float p2 = ex2_approx(fmaf(x[4 * i + 2], cj, -m_use));
-            const float p3 = ex2_approx(fmaf(x[4 * i + 3], cj, -m_use));
-            l0 += p0;
-            l1 += p1;
-            l2 += p2;
-            l3 += p3;
-            pk[i] = pack_e4m3x4(p0 * v_fold, p1 * v_fold, p2 * v_fold, p3 * v_fold);
+            float t0, t1, t2, t3;
+            f32x2_unpack(f32x2_fma(f32x2_pack(x[4 * i], x[4 * i + 1]), c2, nm2), t0, t1);
+            f32x2_unpack(f32x2_fma(f32x2_pack(x[4 * i + 2], x[4 * i + 3]), c2, nm2), t2, t3);
+            const float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
+            const float p2 = ex2_approx(t2), p3 = ex2_approx(t3);
+            s01 = f32x2_add(s01, f32x2_pack(p0, p1));
+            s23 = f32x2_add(s23, f32x2_pack(p2, p3));
+            pk[i] = pack_e4m3x4(p0, p1, p2, p3);
           }
-          ell += (l0 + l1) + (l2 + l3);
+          float a0, a1;
+          f32x2_unpack(f32x2_add(s01, s23), a0, a1);
+          ell += (a0 + a1) / v_fold;
           tmem_st32(tS, pk);
         } else {
           // p = 2^(s*c - m) in pairs.  P is rounded to bf16 for the PV MMA; the
