@@ -110,7 +110,7 @@ struct SmemCtl {
   uint64_t q_full[2];
   uint64_t q_empty[2];
   uint64_t s_full[2];
-  uint64_t p_ready[2];
+  uint64_t p_ready[2][2];   // [tile][half of the block's keys]
   uint64_t o_final[2];
   uint64_t drain;
   uint32_t tmem_base;
@@ -217,7 +217,8 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(bar(ctl.q_full[t]), 1);
       mbar_init(bar(ctl.q_empty[t]), 1);
       mbar_init(bar(ctl.s_full[t]), 1);
-      mbar_init(bar(ctl.p_ready[t]), 128);
+      mbar_init(bar(ctl.p_ready[t][0]), 128);
+      mbar_init(bar(ctl.p_ready[t][1]), 128);
       mbar_init(bar(ctl.o_final[t]), 1);
     }
     mbar_init(bar(ctl.drain), 1);
@@ -316,10 +317,13 @@ __global__ void __launch_bounds__(320, 1)
             mma_f16_ss(tmem + 128 * t, da, db, C::kIdescS, k > 0);
         }
       };
-      auto pv_mma = [&](int t, uint32_t vslot, bool acc) {
+      // O_t += P_t V over the keys of half `hf` of the block (P of each half is
+      // signalled separately, so the first half's product overlaps the
+      // exponentials of the second).
+      auto pv_mma = [&](int t, uint32_t vslot, bool acc, int hf) {
         const uint32_t b0 = sKV + vslot * C::kTileBytes;
 #pragma unroll
-        for (int k = 0; k < C::kPVSteps; ++k) {
+        for (int k = hf * (C::kPVSteps / 2); k < (hf + 1) * (C::kPVSteps / 2); ++k) {
           const uint32_t a = tmem + 128 * t + k * 8;
           if (FP8) {
             const uint64_t db = make_smem_desc(b0 + k * 32, 16, 1024, kSwizzle128B);
@@ -357,9 +361,12 @@ __global__ void __launch_bounds__(320, 1)
           const uint32_t iv = base + 2 * j + 1, ik = base + 2 * j + 2;
           const uint32_t vslot = iv % C::kStages, kslot = ik % C::kStages;
           if (!(ok = wait_item(iv))) break;
-          if (!(ok = wait_bounded(bar(ctl.p_ready[0]), pr[0]++ & 1, wc))) break;
+          if (!(ok = wait_bounded(bar(ctl.p_ready[0][0]), pr[0] & 1, wc))) break;
           tc_fence_after();
-          pv_mma(0, vslot, j > 0);
+          pv_mma(0, vslot, j > 0, 0);
+          if (!(ok = wait_bounded(bar(ctl.p_ready[0][1]), pr[0]++ & 1, wc))) break;
+          tc_fence_after();
+          pv_mma(0, vslot, j > 0, 1);
           if (j == J - 1) mma_commit(bar(ctl.o_final[0]));
           if (j + 1 < J) {
             if (!(ok = wait_item(ik))) break;
@@ -367,9 +374,12 @@ __global__ void __launch_bounds__(320, 1)
             s_mma(0, kslot);
             mma_commit(bar(ctl.s_full[0]));
           }
-          if (!(ok = wait_bounded(bar(ctl.p_ready[1]), pr[1]++ & 1, wc))) break;
+          if (!(ok = wait_bounded(bar(ctl.p_ready[1][0]), pr[1] & 1, wc))) break;
           tc_fence_after();
-          pv_mma(1, vslot, j > 0);
+          pv_mma(1, vslot, j > 0, 0);
+          if (!(ok = wait_bounded(bar(ctl.p_ready[1][1]), pr[1]++ & 1, wc))) break;
+          tc_fence_after();
+          pv_mma(1, vslot, j > 0, 1);
           mma_commit(bar(ctl.kv_empty[vslot]));
           if (j == J - 1) mma_commit(bar(ctl.o_final[1]));
           if (j + 1 < J) {
@@ -493,22 +503,30 @@ __global__ void __launch_bounds__(320, 1)
           const uint64_t c2 = f32x2_pack(cj, cj);
           const uint64_t nm2 = f32x2_pack(-m_f, -m_f);
           uint64_t s01 = 0, s23 = 0;   // (0.f, 0.f)
-          uint32_t pk[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            float t0, t1, t2, t3;
-            f32x2_unpack(f32x2_fma(f32x2_pack(x[4 * i], x[4 * i + 1]), c2, nm2), t0, t1);
-            f32x2_unpack(f32x2_fma(f32x2_pack(x[4 * i + 2], x[4 * i + 3]), c2, nm2), t2, t3);
-            const float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
-            const float p2 = ex2_approx(t2), p3 = ex2_approx(t3);
-            s01 = f32x2_add(s01, f32x2_pack(p0, p1));
-            s23 = f32x2_add(s23, f32x2_pack(p2, p3));
-            pk[i] = pack_e4m3x4(p0, p1, p2, p3);
+          for (int hf = 0; hf < 2; ++hf) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int c = 64 * hf + 4 * i;
+              float t0, t1, t2, t3;
+              f32x2_unpack(f32x2_fma(f32x2_pack(x[c], x[c + 1]), c2, nm2), t0, t1);
+              f32x2_unpack(f32x2_fma(f32x2_pack(x[c + 2], x[c + 3]), c2, nm2), t2, t3);
+              const float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
+              const float p2 = ex2_approx(t2), p3 = ex2_approx(t3);
+              s01 = f32x2_add(s01, f32x2_pack(p0, p1));
+              s23 = f32x2_add(s23, f32x2_pack(p2, p3));
+              pk[i] = pack_e4m3x4(p0, p1, p2, p3);
+            }
+            // keys [64hf, 64hf+64) -> columns [16hf, 16hf+16)
+            tmem_st16(tS + 16 * hf, pk);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar(ctl.p_ready[t][hf]));
           }
           float a0, a1;
           f32x2_unpack(f32x2_add(s01, s23), a0, a1);
           ell += (a0 + a1) / v_fold;
-          tmem_st32(tS, pk);
         } else {
           // p = 2^(s*c - m) in pairs.  P is rounded to bf16 for the PV MMA; the
           // sum of exactly those rounded values (l~) normalises O, so numerator
@@ -537,16 +555,19 @@ __global__ void __launch_bounds__(320, 1)
               ex0 = f32x2_add(ex0, e);
             }
           }
+          tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+          tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+          // bf16: one signal for both halves of the keys (a half's PV is as long
+          // as the exponentials it could overlap; the extra wait costs more).
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(bar(ctl.p_ready[t][0]));
+          mbar_arrive(bar(ctl.p_ready[t][1]));
           float b0, b1;
           f32x2_unpack(f32x2_add(ex0, ex1), b0, b1);
           ell_r += (r0 + r1) + (r2 + r3);
           ell += b0 + b1;
-          tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-          tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
         }
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(bar(ctl.p_ready[t]));
       }
       if (!ok) break;
       // ---------------------------------------------------------- epilogue
