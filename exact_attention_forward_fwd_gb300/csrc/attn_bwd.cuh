@@ -93,7 +93,9 @@ struct BwdCtl {
   uint64_t empty[16];      // ring slot free
   uint64_t fix_full;       // the unit's fixed tiles (K, V or Q, dO) loaded
   uint64_t fix_empty;      // ... free again
-  uint64_t s_full;         // S and dP of a block computed
+  uint64_t s_full;         // S (dK/dV: S^T) of a block computed
+  uint64_t dp_full;        // dP (dK/dV: dP^T) of a block computed
+  uint64_t s_buf[2];       // dQ kernel: S of a block computed, per S buffer (block parity)
   uint64_t p_ready;        // dK/dV: P^T written; dQ: dS written (16 warp arrivals)
   uint64_t ds_ready;       // dK/dV: dS^T written (16 warp arrivals)
   uint64_t unit_done;      // the unit's accumulators final
@@ -151,6 +153,7 @@ __global__ void __launch_bounds__(576, 1)
     mbar_init(bar(ctl.fix_full), 1);
     mbar_init(bar(ctl.fix_empty), 1);
     mbar_init(bar(ctl.s_full), 1);
+    mbar_init(bar(ctl.dp_full), 1);
     mbar_init(bar(ctl.p_ready), C::kEW);
     mbar_init(bar(ctl.ds_ready), C::kEW);
     mbar_init(bar(ctl.unit_done), 1);
@@ -272,8 +275,9 @@ __global__ void __launch_bounds__(576, 1)
         if (!(ok = wait_slot(base) && wait_slot(base + 1))) break;
         tc_fence_after();
         ss(0, sK, sRing + (base % C::kStages) * C::kTile);
-        ss(128, sV, sRing + ((base + 1) % C::kStages) * C::kTile);
         mma_commit(bar(ctl.s_full));
+        ss(128, sV, sRing + ((base + 1) % C::kStages) * C::kTile);
+        mma_commit(bar(ctl.dp_full));
         for (int t = 0; t < T && ok; ++t, ++gblk) {
           const uint32_t iq = base + 2 * t, io = iq + 1;
           const uint32_t sQ = sRing + (iq % C::kStages) * C::kTile;
@@ -289,6 +293,7 @@ __global__ void __launch_bounds__(576, 1)
             if (!(ok = wait_slot(iq + 2))) break;
             tc_fence_after();
             ss(0, sK, sRing + ((iq + 2) % C::kStages) * C::kTile);
+            mma_commit(bar(ctl.s_full));   // P^T(t+1) can start during dK(t), dP^T(t+1)
           }
           // dK += dS^T Q once dS^T is written
           if (!(ok = wait_bounded(bar(ctl.ds_ready), gblk & 1, wc))) break;
@@ -299,7 +304,7 @@ __global__ void __launch_bounds__(576, 1)
             if (!(ok = wait_slot(io + 2))) break;
             tc_fence_after();
             ss(128, sV, sRing + ((io + 2) % C::kStages) * C::kTile);
-            mma_commit(bar(ctl.s_full));
+            mma_commit(bar(ctl.dp_full));
           }
         }
         mma_commit(bar(ctl.unit_done));
@@ -379,7 +384,11 @@ __global__ void __launch_bounds__(576, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(ctl.p_ready));
-        // ---- phase B: dS^T = P^T o (dP^T - D)
+        // ---- phase B: dS^T = P^T o (dP^T - D), once dP^T is computed
+        ok = wait_bounded(bar(ctl.dp_full), gblk & 1, wc);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
         {
           uint32_t dv[32];
           tmem_ld32(tmem + lane_off + 128 + 32 * h, dv);
@@ -481,6 +490,9 @@ __global__ void __launch_bounds__(576, 1)
     mbar_init(bar(ctl.fix_full), 1);
     mbar_init(bar(ctl.fix_empty), 1);
     mbar_init(bar(ctl.s_full), 1);
+    mbar_init(bar(ctl.s_buf[0]), 1);
+    mbar_init(bar(ctl.s_buf[1]), 1);
+    mbar_init(bar(ctl.dp_full), 1);
     mbar_init(bar(ctl.p_ready), C::kEW);
     mbar_init(bar(ctl.ds_ready), C::kEW);
     mbar_init(bar(ctl.unit_done), 1);
@@ -588,8 +600,9 @@ __global__ void __launch_bounds__(576, 1)
         if (!(ok = wait_slot(base) && wait_slot(base + 1))) break;
         tc_fence_after();
         ss(sbuf(g0), sQ, slot_addr(base));
+        mma_commit(bar(ctl.s_buf[g0 & 1]));
         ss(kColDP, sdO, slot_addr(base + 1));
-        mma_commit(bar(ctl.s_full));
+        mma_commit(bar(ctl.dp_full));
         mma_commit(bar(ctl.empty[(base + 1) % C::kStagesDQ]));   // V_0 done
         for (int jj = 0; jj < J && ok; ++jj, ++gblk) {
           const uint32_t ik = base + 2 * jj;
@@ -599,6 +612,9 @@ __global__ void __launch_bounds__(576, 1)
             if (!(ok = wait_slot(ik + 2))) break;
             tc_fence_after();
             ss(sbuf(gblk + 1), sQ, slot_addr(ik + 2));
+            // Its own barrier per buffer: this commit can come before the
+            // element-wise pass has waited for S(jj), one block earlier.
+            mma_commit(bar(ctl.s_buf[(gblk + 1) & 1]));
           }
           if (!(ok = wait_bounded(bar(ctl.p_ready), gblk & 1, wc))) break;
           tc_fence_after();
@@ -607,7 +623,7 @@ __global__ void __launch_bounds__(576, 1)
             if (!(ok = wait_slot(ik + 3))) break;
             tc_fence_after();
             ss(kColDP, sdO, slot_addr(ik + 3));
-            mma_commit(bar(ctl.s_full));
+            mma_commit(bar(ctl.dp_full));
             mma_commit(bar(ctl.empty[(ik + 3) % C::kStagesDQ]));   // V_{jj+1} done
           }
           // dQ += dS K_j (K_j as MN-major B)
@@ -648,37 +664,51 @@ __global__ void __launch_bounds__(576, 1)
         const int k0 = jj * 128 + 32 * h;   // first key of this thread's columns
         const bool full_vis = (jj * 128 + 127 < p.N) && (!p.causal || jj * 128 + 127 <= i * 128) &&
                               (p.window <= 0 || jj * 128 > i * 128 + 127 - p.window);
-        ok = wait_bounded(bar(ctl.s_full), gblk & 1, wc);
+        // Exponentials as soon as S is there; dS once dP is there too.
+        ok = wait_bounded(bar(ctl.s_buf[gblk & 1]), (gblk >> 1) & 1, wc);
         ok = __all_sync(0xffffffffu, ok);
         ok = bar_and(1, 32 * C::kEW, ok);
         if (!ok) break;
         tc_fence_after();
         const uint32_t scol = sbuf(gblk) + 32 * h;
-        uint32_t sv[32], dv[32];
-        tmem_ld32(tmem + lane_off + scol, sv);
+        float pr[32];
+        {
+          uint32_t sv[32];
+          tmem_ld32(tmem + lane_off + scol, sv);
+          tmem_wait_ld();
+          reg_fence(sv);
+          if (!full_vis) {
+            // Diagonal / window-edge / ragged block: 2^-inf = 0 for invisible scores.
+#pragma unroll
+            for (int col = 0; col < 32; ++col)
+              if (!bwd_visible(k0 + col, q, p)) sv[col] = 0xff800000u;
+          }
+          const uint64_t c2 = f32x2_pack(cl, cl);
+          const uint64_t nl2 = f32x2_pack(-Lq, -Lq);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            float a0, a1;
+            f32x2_unpack(f32x2_fma(f32x2_pack(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), c2, nl2),
+                         a0, a1);
+            pr[2 * e] = ex2_approx(a0);
+            pr[2 * e + 1] = ex2_approx(a1);
+          }
+        }
+        ok = wait_bounded(bar(ctl.dp_full), gblk & 1, wc);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t dv[32];
         tmem_ld32(tmem + lane_off + kColDP + 32 * h, dv);
         tmem_wait_ld();
-        reg_fence(sv);
         reg_fence(dv);
-        if (!full_vis) {
-          // Diagonal / window-edge / ragged block: zero the invisible scores'
-          // probabilities through their exponent (2^-inf = 0).
-#pragma unroll
-          for (int col = 0; col < 32; ++col)
-            if (!bwd_visible(k0 + col, q, p)) sv[col] = 0xff800000u;
-        }
-        const uint64_t c2 = f32x2_pack(cl, cl);
-        const uint64_t nl2 = f32x2_pack(-Lq, -Lq);
         const uint64_t nd2 = f32x2_pack(-Dq, -Dq);
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          float a0, a1, g0, g1;
-          f32x2_unpack(f32x2_fma(f32x2_pack(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), c2, nl2),
-                       a0, a1);
-          f32x2_unpack(f32x2_add(f32x2_pack(__uint_as_float(dv[2 * e]), __uint_as_float(dv[2 * e + 1])), nd2),
-                       g0, g1);
-          pk[e] = pack_bf16x2(ex2_approx(a0) * g0, ex2_approx(a1) * g1);
+          float g0, g1;
+          f32x2_unpack(f32x2_add(f32x2_pack(__uint_as_float(dv[2 * e]), __uint_as_float(dv[2 * e + 1])), nd2), g0, g1);
+          pk[e] = pack_bf16x2(pr[2 * e] * g0, pr[2 * e + 1] * g1);
         }
         // dS of keys [32h, +32) -> columns [32h, 32h+16) of this S buffer
         tmem_st16(tmem + lane_off + scol, pk);
