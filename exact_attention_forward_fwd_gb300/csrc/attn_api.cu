@@ -273,6 +273,8 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   float* dd = reinterpret_cast<float*>(static_cast<char*>(workspace) + half);
   p.lp = lp;
   p.dd = dd;
+  p.q = static_cast<const uint16_t*>(q);
+  p.dO = static_cast<const uint16_t*>(dO);
   p.dq = dq;
   p.dk = dk;
   p.dv = dv;

@@ -43,6 +43,8 @@ namespace gb300 {
 struct BwdParams {
   const float* lp;       // [BH][Npad] L * log2(e) (+inf past N)
   const float* dd;       // [BH][Npad] D = rowdot(dO, O) (0 past N)
+  const uint16_t* q;     // bf16 [BH][N][D] (read directly by the dQ kernel)
+  const uint16_t* dO;    // bf16 [BH][N][D]
   void* dq;              // bf16 [BH][N][D]
   void* dk;              // bf16 [BHk][N][D]
   void* dv;              // bf16 [BHk][N][D]
@@ -64,13 +66,12 @@ struct BCfg {
   static constexpr int kTile = 128 * D * 2;                 // 128 rows x D bf16
   static constexpr int kSlabs = D / 64;                     // 128-byte column slabs
   // Ring of tiles: dK/dV kernel Q/dO tiles (+ L', D of each Q tile's block);
-  // dQ kernel K/V tiles (5 slots at D = 128: K_{j+2} can load while K_j, V_j+1,
-  // K_j+1 are in use).
+  // dQ kernel K/V tiles (its Q and dO live in TMEM, so the ring gets the rest).
   static constexpr int kStages = (D == 128) ? 4 : 8;
-  static constexpr int kStagesDQ = (D == 128) ? 5 : 10;
+  static constexpr int kStagesDQ = (D == 128) ? 6 : 12;
   static constexpr int kStatBytes = 2 * 128 * 4;            // L' and D of one query block
   static constexpr int kSmemBytes = (2 + kStages) * kTile + kStages * kStatBytes + 1024;
-  static constexpr int kSmemBytesDQ = (2 + kStagesDQ) * kTile + 1024;
+  static constexpr int kSmemBytesDQ = kStagesDQ * kTile + 1024;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr int kEW = 16;                            // element-wise warps
   static constexpr int kThreads = (kEW + 2) * 32;
@@ -95,7 +96,7 @@ struct BwdCtl {
   uint64_t fix_empty;      // ... free again
   uint64_t s_full;         // S (dK/dV: S^T) of a block computed
   uint64_t dp_full;        // dP (dK/dV: dP^T) of a block computed
-  uint64_t s_buf[2];       // dQ kernel: S of a block computed, per S buffer (block parity)
+  uint64_t s_read;         // dQ kernel: S of a block read by all element-wise warps
   uint64_t p_ready;        // dK/dV: P^T written; dQ: dS written (16 warp arrivals)
   uint64_t ds_ready;       // dK/dV: dS^T written (16 warp arrivals)
   uint64_t unit_done;      // the unit's accumulators final
@@ -462,7 +463,11 @@ __global__ void __launch_bounds__(576, 1)
 }
 
 // ============================================================================
-// dQ: one unit = (batch * query head, 128-query block i).
+// dQ: one unit = (batch * query head, 128-query block i).  Q_i and dO_i stay in
+// TMEM for the whole unit (written by the element-wise warps from global
+// memory), so S = Q K^T and dP = dO V^T are TS products that read only K_j and
+// V_j from shared memory.  TMEM: Q [0, D/2), dO [D/2, D) (bf16 pairs), S
+// [D, D+128), dP [D+128, D+256) with dS (bf16) written over it, dQ after that.
 // ============================================================================
 template <int D>
 __global__ void __launch_bounds__(576, 1)
@@ -474,27 +479,22 @@ __global__ void __launch_bounds__(576, 1)
   __shared__ BwdCtl ctl;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  const uint32_t sQ = smem_addr(smem);
-  const uint32_t sdO = sQ + C::kTile;
-  const uint32_t sRing = sdO + C::kTile;    // K_j / V_j tiles, alternating
+  const uint32_t sRing = smem_addr(smem);   // K_j / V_j tiles, alternating
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   auto bar = [&](uint64_t& b) { return smem_addr(&b); };
-  constexpr uint32_t kColDP = 128, kColDQ = 256, kColS1 = 384;
+  constexpr uint32_t kColQ = 0, kColdO = D / 2, kColS = D, kColDP = D + 128, kColDQ = D + 256;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStagesDQ; ++s) {
       mbar_init(bar(ctl.full[s]), 1);
       mbar_init(bar(ctl.empty[s]), 1);
     }
-    mbar_init(bar(ctl.fix_full), 1);
-    mbar_init(bar(ctl.fix_empty), 1);
+    mbar_init(bar(ctl.fix_full), C::kEW);   // Q_i, dO_i written into TMEM
     mbar_init(bar(ctl.s_full), 1);
-    mbar_init(bar(ctl.s_buf[0]), 1);
-    mbar_init(bar(ctl.s_buf[1]), 1);
     mbar_init(bar(ctl.dp_full), 1);
-    mbar_init(bar(ctl.p_ready), C::kEW);
-    mbar_init(bar(ctl.ds_ready), C::kEW);
+    mbar_init(bar(ctl.s_read), C::kEW);     // S read: its columns may be overwritten
+    mbar_init(bar(ctl.p_ready), C::kEW);    // dS written
     mbar_init(bar(ctl.unit_done), 1);
     mbar_init(bar(ctl.drain), 1);
     ctl.abort_flag = 0;
@@ -526,31 +526,21 @@ __global__ void __launch_bounds__(576, 1)
     const int b = bh / p.H, hq = bh - (bh / p.H) * p.H;
     return b * p.Hk + hq / p.group;
   };
-  auto sbuf = [&](uint32_t gg) { return (gg & 1) ? kColS1 : 0u; };
 
   if (warp == C::kEW) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      prefetch_tensormap(&tmQ);
       prefetch_tensormap(&tmK);
       prefetch_tensormap(&tmV);
-      prefetch_tensormap(&tmdO);
-      const uint64_t pol_fix = l2_policy_evict_first();
       const uint64_t pol_ring = l2_policy_evict_last();
-      uint32_t item = 0, uit = 0;
+      uint32_t item = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uit) {
+      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
         int bh, i;
         unit(u, bh, i);
         int j_lo, j_hi;
         bwd_krange(i, p, j_lo, j_hi);
         const int bhk = kv_head(bh);
-        if (uit > 0 && !(ok = wait_bounded(bar(ctl.fix_empty), (uit - 1) & 1, wc))) break;
-        mbar_arrive_expect_tx(bar(ctl.fix_full), 2 * C::kTile);
-        for (int s = 0; s < C::kSlabs; ++s) {
-          tma_load_3d_hint(sQ + s * 16384, &tmQ, bar(ctl.fix_full), s * 64, i * 128, bh, pol_fix);
-          tma_load_3d_hint(sdO + s * 16384, &tmdO, bar(ctl.fix_full), s * 64, i * 128, bh, pol_fix);
-        }
         for (int jj = j_lo; jj <= j_hi && ok; ++jj) {
           for (int w2 = 0; w2 < 2 && ok; ++w2, ++item) {   // K_j, then V_j
             const uint32_t slot = item % C::kStagesDQ;
@@ -567,7 +557,6 @@ __global__ void __launch_bounds__(576, 1)
         const uint32_t last = s + ((issued - 1 - s) / C::kStagesDQ) * C::kStagesDQ;
         wait_bounded(bar(ctl.full[s]), (last / C::kStagesDQ) & 1, wc, false);
       }
-      if (uit > 0) wait_bounded(bar(ctl.fix_full), (uit - 1) & 1, wc, false);
     }
   } else if (warp == C::kEW + 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -577,68 +566,63 @@ __global__ void __launch_bounds__(576, 1)
       auto wait_slot = [&](uint32_t it) {
         return wait_bounded(bar(ctl.full[it % C::kStagesDQ]), (it / C::kStagesDQ) & 1, wc);
       };
-      auto ss = [&](uint32_t d_col, uint32_t a0, uint32_t b0) {
+      auto slot_addr = [&](uint32_t it) { return sRing + (it % C::kStagesDQ) * C::kTile; };
+      // [128 rows in TMEM at a_col] x [128 rows of the K-major tile b0]^T over K = D
+      auto ts_k = [&](uint32_t d_col, uint32_t a_col, uint32_t b0) {
 #pragma unroll
         for (int k = 0; k < C::kSSteps; ++k) {
           const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-          mma_f16_ss(tmem + d_col, make_smem_desc(a0 + off, 16, 1024, kSwizzle128B),
-                     make_smem_desc(b0 + off, 16, 1024, kSwizzle128B), C::kIdescSS, k > 0);
+          mma_f16_ts(tmem + d_col, tmem + a_col + 8 * k, make_smem_desc(b0 + off, 16, 1024, kSwizzle128B),
+                     C::kIdescSS, k > 0 ? 1u : 0u);
         }
       };
-      auto slot_addr = [&](uint32_t it) { return sRing + (it % C::kStagesDQ) * C::kTile; };
       for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uit) {
         int bh, i;
         unit(u, bh, i);
         int j_lo, j_hi;
         bwd_krange(i, p, j_lo, j_hi);
         const int J = j_hi - j_lo + 1;
-        if (!(ok = wait_bounded(bar(ctl.fix_full), uit & 1, wc))) break;
+        if (!(ok = wait_bounded(bar(ctl.fix_full), uit & 1, wc))) break;   // Q_i, dO_i in TMEM
         const uint32_t base = item;            // K_j item = base + 2jj, V_j = base + 2jj + 1
         item += 2 * J;
-        const uint32_t g0 = gblk;
-        // prologue: S(0), dP(0)
         if (!(ok = wait_slot(base) && wait_slot(base + 1))) break;
         tc_fence_after();
-        ss(sbuf(g0), sQ, slot_addr(base));
-        mma_commit(bar(ctl.s_buf[g0 & 1]));
-        ss(kColDP, sdO, slot_addr(base + 1));
+        ts_k(kColS, kColQ, slot_addr(base));
+        mma_commit(bar(ctl.s_full));
+        ts_k(kColDP, kColdO, slot_addr(base + 1));
         mma_commit(bar(ctl.dp_full));
         mma_commit(bar(ctl.empty[(base + 1) % C::kStagesDQ]));   // V_0 done
         for (int jj = 0; jj < J && ok; ++jj, ++gblk) {
           const uint32_t ik = base + 2 * jj;
           const bool more = jj + 1 < J;
-          // S(jj+1) into the other buffer while the element-wise pass of jj runs
+          // S(jj+1) once the element-wise pass has read S(jj)
           if (more) {
-            if (!(ok = wait_slot(ik + 2))) break;
+            if (!(ok = wait_bounded(bar(ctl.s_read), gblk & 1, wc) && wait_slot(ik + 2))) break;
             tc_fence_after();
-            ss(sbuf(gblk + 1), sQ, slot_addr(ik + 2));
-            // Its own barrier per buffer: this commit can come before the
-            // element-wise pass has waited for S(jj), one block earlier.
-            mma_commit(bar(ctl.s_buf[(gblk + 1) & 1]));
+            ts_k(kColS, kColQ, slot_addr(ik + 2));
+            mma_commit(bar(ctl.s_full));
           }
+          // dQ += dS K_j once dS is written (over dP)
           if (!(ok = wait_bounded(bar(ctl.p_ready), gblk & 1, wc))) break;
           tc_fence_after();
-          // dP(jj+1): the dP columns were read by the element-wise pass of jj
-          if (more) {
-            if (!(ok = wait_slot(ik + 3))) break;
-            tc_fence_after();
-            ss(kColDP, sdO, slot_addr(ik + 3));
-            mma_commit(bar(ctl.dp_full));
-            mma_commit(bar(ctl.empty[(ik + 3) % C::kStagesDQ]));   // V_{jj+1} done
-          }
-          // dQ += dS K_j (K_j as MN-major B)
-          const uint32_t a_col = sbuf(gblk);
           const uint32_t kb = slot_addr(ik);
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
-            const uint32_t a = tmem + a_col + (k >> 1) * 32 + (k & 1) * 8;
+            const uint32_t a = tmem + kColDP + (k >> 1) * 32 + (k & 1) * 8;
             mma_f16_ts(tmem + kColDQ, a, make_smem_desc(kb + k * 2048, 16384, 1024, kSwizzle128B),
                        C::kIdescTS, (jj > 0 || k > 0) ? 1u : 0u);
           }
           mma_commit(bar(ctl.empty[ik % C::kStagesDQ]));   // K_j done
+          // dP(jj+1) over dS(jj): after dQ(jj) in issue order
+          if (more) {
+            if (!(ok = wait_slot(ik + 3))) break;
+            tc_fence_after();
+            ts_k(kColDP, kColdO, slot_addr(ik + 3));
+            mma_commit(bar(ctl.dp_full));
+            mma_commit(bar(ctl.empty[(ik + 3) % C::kStagesDQ]));   // V_{jj+1} done
+          }
         }
         mma_commit(bar(ctl.unit_done));
-        mma_commit(bar(ctl.fix_empty));
       }
       mma_commit(bar(ctl.drain));
       wait_bounded(bar(ctl.drain), 0, wc, false);
@@ -646,7 +630,7 @@ __global__ void __launch_bounds__(576, 1)
   } else {
     // ------------------------------------------------------------ element-wise
     const int qd = warp & 3;             // TMEM lane quarter: queries 32qd .. 32qd+31
-    const int h = warp >> 2;             // keys [32h, 32h+32) of each block
+    const int h = warp >> 2;             // keys [32h, 32h+32) of each block; head dims [D/4 h, +D/4)
     const int r = qd * 32 + lane;        // query row within the block
     const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
     const float cl = p.scale_log2;
@@ -660,23 +644,55 @@ __global__ void __launch_bounds__(576, 1)
       const int q = i * 128 + r;
       const float Lq = __ldg(p.lp + (size_t)bh * p.Npad + q);   // +inf past N: P = 0
       const float Dq = __ldg(p.dd + (size_t)bh * p.Npad + q);
+      // Q_i and dO_i rows into TMEM (zeros past N).  The previous unit's products
+      // that read them are complete: its unit_done was waited for.
+      {
+        constexpr int kE = D / 4;   // elements of this thread: [kE h, kE h + kE)
+        uint32_t qv[kE / 2], ov[kE / 2];
+        if (q < p.N) {
+          const uint4* sq = reinterpret_cast<const uint4*>(p.q + ((size_t)bh * p.N + q) * D + kE * h);
+          const uint4* so = reinterpret_cast<const uint4*>(p.dO + ((size_t)bh * p.N + q) * D + kE * h);
+#pragma unroll
+          for (int e = 0; e < kE / 8; ++e) {
+            const uint4 a = __ldg(sq + e), c = __ldg(so + e);
+            qv[4 * e] = a.x; qv[4 * e + 1] = a.y; qv[4 * e + 2] = a.z; qv[4 * e + 3] = a.w;
+            ov[4 * e] = c.x; ov[4 * e + 1] = c.y; ov[4 * e + 2] = c.z; ov[4 * e + 3] = c.w;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < kE / 2; ++e) qv[e] = ov[e] = 0u;
+        }
+        if (kE == 32) {
+          tmem_st16(tmem + lane_off + kColQ + 16 * h, *reinterpret_cast<const uint32_t(*)[16]>(qv));
+          tmem_st16(tmem + lane_off + kColdO + 16 * h, *reinterpret_cast<const uint32_t(*)[16]>(ov));
+        } else {
+          tmem_st8(tmem + lane_off + kColQ + 8 * h, *reinterpret_cast<const uint32_t(*)[8]>(qv));
+          tmem_st8(tmem + lane_off + kColdO + 8 * h, *reinterpret_cast<const uint32_t(*)[8]>(ov));
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(ctl.fix_full));
+      }
       for (int jj = j_lo; jj <= j_hi; ++jj, ++gblk) {
         const int k0 = jj * 128 + 32 * h;   // first key of this thread's columns
         const bool full_vis = (jj * 128 + 127 < p.N) && (!p.causal || jj * 128 + 127 <= i * 128) &&
                               (p.window <= 0 || jj * 128 > i * 128 + 127 - p.window);
         // Exponentials as soon as S is there; dS once dP is there too.
-        ok = wait_bounded(bar(ctl.s_buf[gblk & 1]), (gblk >> 1) & 1, wc);
+        ok = wait_bounded(bar(ctl.s_full), gblk & 1, wc);
         ok = __all_sync(0xffffffffu, ok);
         ok = bar_and(1, 32 * C::kEW, ok);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t scol = sbuf(gblk) + 32 * h;
         float pr[32];
         {
           uint32_t sv[32];
-          tmem_ld32(tmem + lane_off + scol, sv);
+          tmem_ld32(tmem + lane_off + kColS + 32 * h, sv);
           tmem_wait_ld();
           reg_fence(sv);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(ctl.s_read));   // S(jj+1) may overwrite S now
           if (!full_vis) {
             // Diagonal / window-edge / ragged block: 2^-inf = 0 for invisible scores.
 #pragma unroll
@@ -710,8 +726,8 @@ __global__ void __launch_bounds__(576, 1)
           f32x2_unpack(f32x2_add(f32x2_pack(__uint_as_float(dv[2 * e]), __uint_as_float(dv[2 * e + 1])), nd2), g0, g1);
           pk[e] = pack_bf16x2(pr[2 * e] * g0, pr[2 * e + 1] * g1);
         }
-        // dS of keys [32h, +32) -> columns [32h, 32h+16) of this S buffer
-        tmem_st16(tmem + lane_off + scol, pk);
+        // dS of keys [32h, +32) -> columns [32h, 32h+16) of the dP region (read above)
+        tmem_st16(tmem + lane_off + kColDP + 32 * h, pk);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
