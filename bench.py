@@ -355,8 +355,9 @@ def run_mine(args):
     # seven, recomputing S and dP for dQ instead of adding it atomically).
     bwd = None
     if not args.no_extra:
+        io_mib = 5 * w.B * w.H * w.N * w.d * 2 / 2 ** 20
         bwd = {"flops_convention": "2.5 x forward FLOPs (5 tile products); the kernels execute 7",
-               "l2": "Q, K, V, O, dO 320 MiB > 129 MB L2 (no flush)"}
+               "l2": f"Q, K, V, O, dO {io_mib:.0f} MiB (L2 129 MB; no flush)"}
         g = torch.Generator().manual_seed(w.seed + 60)
         dO = torch.randn(w.B, w.H, w.N, w.d, generator=g).to(torch.bfloat16).to(dev)
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
