@@ -66,6 +66,15 @@ AttnParams base_params(void* o, float* lse, int B, int H, int H_kv, int N, float
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.timeout_ns = kDefaultTimeoutNs;
   p.splits = 1;
+  // Causal order: groups of heads whose K and V (bf16, head dim <= 128) take at
+  // most 48 MiB, well inside the 129 MB L2 next to the Q and O streams.
+  {
+    const long long kv_bytes = 4LL * N * 128;
+    long long hg = (48LL << 20) / (kv_bytes > 0 ? kv_bytes : 1);
+    if (hg < 1) hg = 1;
+    if (hg > BH) hg = BH;
+    p.hgroup = static_cast<int>(hg);
+  }
   return p;
 }
 

@@ -49,6 +49,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "ptx.cuh"
 
@@ -79,6 +80,8 @@ struct AttnParams {
   // `splits` contiguous key ranges, each a unit of its own, and each unit writes
   // its partial result: O normalised by its own denominator, and its own
   // logsumexp.  A merge kernel combines them.
+  int hgroup;            // causal order: heads per group (K/V of a group stay in L2)
+  int* sched;            // unit counter for dynamic scheduling (zeroed before launch), or null
   int splits;            // key ranges per (head, pair); 1 without split-KV
   float* o_part;         // [splits][BH][N][D] fp32, or null
   float* lse_part;       // [splits][BH][N] fp32 (natural log), or null
@@ -113,6 +116,9 @@ struct SmemCtl {
   uint64_t p_ready[2][2];   // [tile][half of the block's keys]
   uint64_t o_final[2];
   uint64_t drain;
+  uint64_t unit_full[4];    // ring of work-unit indices handed out by the load warp
+  uint64_t unit_empty[4];
+  int unit_ring[4];
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -153,9 +159,12 @@ struct Unit {
 
 // Work unit u -> (head, query-tile pair, key blocks to visit).  Non-causal:
 // consecutive units walk the pairs of one head (K/V of a head stay hot in L2).
-// Causal: longest first -- all heads' last pair, then the one before, ...; a
-// sliding window also skips the key blocks entirely before the window of the
-// pair's first row.  Query head h of batch b reads KV head h / group.  With
+// Causal: longest first within groups of `hgroup` heads -- the group's last
+// pairs, then the ones before, ...; the groups one after the other, so that
+// only one group's K/V (sized by the host to fit L2) is live at a time.  The
+// units are handed out dynamically, so the short units at the end of a group
+// do not unbalance the SMs.  A sliding window also skips the key blocks
+// entirely before the window of the pair's first row.  Query head h of batch b reads KV head h / group.  With
 // split-KV, consecutive units are the key ranges of one pair: range s takes
 // blocks [s*nb/S, (s+1)*nb/S) of the pair's nb visible blocks (empty when
 // nb < S; such a unit only writes an empty partial result).
@@ -168,8 +177,13 @@ __device__ __forceinline__ Unit unit_of(int u, const AttnParams& p) {
     u /= S;
   }
   if (p.causal) {
-    const int r = u / p.BH;
-    w.bh = u - r * p.BH;
+    const int HG = p.hgroup > 0 ? p.hgroup : p.BH;
+    const int per_group = HG * p.npairs;
+    const int g = u / per_group;
+    const int v = u - g * per_group;
+    const int hg = min(HG, p.BH - g * HG);   // heads in this group (the last may have fewer)
+    const int r = v / hg;
+    w.bh = g * HG + (v - r * hg);
     w.pair = p.npairs - 1 - r;
     const int j_hi = min(p.nkb - 1, 2 * w.pair + 1);
     w.j0 = p.window > 0 ? max(0, w.pair * 256 - p.window + 1) / 128 : 0;
@@ -222,6 +236,10 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(bar(ctl.o_final[t]), 1);
     }
     mbar_init(bar(ctl.drain), 1);
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(bar(ctl.unit_full[s]), 1);
+      mbar_init(bar(ctl.unit_empty[s]), 9);   // the MMA thread and the 8 softmax warps
+    }
     ctl.abort_flag = 0;
     fence_mbarrier_init();
     fence_proxy_async_smem();
@@ -236,6 +254,29 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t tmem = ctl.tmem_base;
   const WaitCtx wc{&ctl.abort_flag, p.status ? p.status : &g_attn_status, p.timeout_ns};
 
+  // Work units: the load warp takes the next index (atomic counter, or the
+  // static stride without one) and passes it through a 4-entry ring; -1 ends.
+  auto publish_unit = [&](uint32_t k, bool& ok) -> int {
+    int u = p.sched ? atomicAdd(p.sched, 1) : static_cast<int>(blockIdx.x + k * gridDim.x);
+    if (u >= p.num_units) u = -1;
+    const uint32_t slot = k & 3;
+    if (k >= 4 && !(ok = wait_bounded(bar(ctl.unit_empty[slot]), ((k >> 2) - 1) & 1, wc))) return -1;
+    ctl.unit_ring[slot] = u;
+    mbar_arrive(bar(ctl.unit_full[slot]));
+    return u;
+  };
+  // Consumer side (whole warp, or the MMA thread alone with `single`).
+  auto take_unit = [&](uint32_t k, bool& ok, bool single) -> int {
+    const uint32_t slot = k & 3;
+    ok = wait_bounded(bar(ctl.unit_full[slot]), (k >> 2) & 1, wc);
+    if (!single) ok = __all_sync(0xffffffffu, ok);
+    if (!ok) return -1;
+    const int u = *reinterpret_cast<volatile int*>(&ctl.unit_ring[slot]);
+    if (!single) __syncwarp();
+    if (single || lane == 0) mbar_arrive(bar(ctl.unit_empty[slot]));
+    return u;
+  };
+
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -249,7 +290,9 @@ __global__ void __launch_bounds__(320, 1)
       uint32_t qn[2] = {0, 0};  // Q tiles issued per tile slot
       bool ok = true;
       int loads = 0;
-      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+      for (uint32_t k = 0; ok; ++k) {
+        const int u = publish_unit(k, ok);
+        if (u < 0) break;
         const Unit w = unit_of(u, p);
         if (w.nblocks == 0) continue;   // empty key range (split-KV)
         for (int t = 0; t < 2 && ok; ++t) {
@@ -337,7 +380,9 @@ __global__ void __launch_bounds__(320, 1)
       auto wait_item = [&](uint32_t it) {
         return wait_bounded(bar(ctl.kv_full[it % C::kStages]), (it / C::kStages) & 1, wc);
       };
-      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+      for (uint32_t k = 0; ok; ++k) {
+        const int u = take_unit(k, ok, true);
+        if (u < 0) break;
         const Unit w = unit_of(u, p);
         const int J = w.nblocks;
         if (J == 0) continue;   // empty key range (split-KV)
@@ -410,7 +455,9 @@ __global__ void __launch_bounds__(320, 1)
     const float NEG_INF = __int_as_float(0xff800000);
     uint32_t sit = 0, uit = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+    for (uint32_t k = 0; ok; ++k) {
+      const int u = take_unit(k, ok, false);
+      if (u < 0) break;
       const Unit w = unit_of(u, p);
       const int row = w.pair * 256 + t * 128 + r;
       if (w.nblocks == 0) {
@@ -640,6 +687,35 @@ namespace gb300 {
 
 // Host-side launch of one instantiation (defined in this header so that each
 // translation unit instantiates exactly one configuration).
+// Unit counters of the dynamic scheduler (one file-scope array per translation
+// unit).  Each launch takes the next of 64 counters in turn and zeroes it on
+// its stream first, so launches in flight on different streams do not share a
+// counter (unless 64 of them overlap).
+static __device__ int g_unit_counter[64];
+
+static cudaError_t unit_counter(cudaStream_t stream, int** out) {
+  static std::mutex mu;
+  static int* base[64] = {};
+  static unsigned next = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  int* c = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (base[dev] == nullptr) {
+      void* a = nullptr;
+      if ((e = cudaGetSymbolAddress(&a, g_unit_counter)) != cudaSuccess) return e;
+      base[dev] = static_cast<int*>(a);
+    }
+    c = base[dev] + (next++ % 64);
+  }
+  if ((e = cudaMemsetAsync(c, 0, sizeof(int), stream)) != cudaSuccess) return e;
+  *out = c;
+  return cudaSuccess;
+}
+
 template <int D, bool FP8>
 cudaError_t launch_attn(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                         const AttnParams& p, int grid, cudaStream_t stream) {
@@ -648,12 +724,14 @@ cudaError_t launch_attn(const CUtensorMap& q, const CUtensorMap& k, const CUtens
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
+  AttnParams pd = p;
+  if ((e = unit_counter(stream, &pd.sched)) != cudaSuccess) return e;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(C::kThreads);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = stream;
-  return cudaLaunchKernelEx(&cfg, kern, q, k, v, p);
+  return cudaLaunchKernelEx(&cfg, kern, q, k, v, pd);
 }
 
 // Status word of this translation unit's kernels.

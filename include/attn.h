@@ -27,6 +27,11 @@
  *   - Every bounded wait inside a kernel gives up after a time limit (1 s for
  *     the plain entry points), records ATTN_ERR_TIMEOUT, frees its tensor
  *     memory and returns; outputs are then unspecified.
+ *   - The forward kernels hand out their work units dynamically from a counter
+ *     in the library's own device memory (64 counters used in turn, each zeroed
+ *     by a memset on the caller's stream before its launch; no allocation).
+ *     The first call on a device looks the counters up (cudaGetSymbolAddress):
+ *     make one call before capturing a stream into a CUDA graph.
  */
 #ifndef GB300_ATTN_H
 #define GB300_ATTN_H
