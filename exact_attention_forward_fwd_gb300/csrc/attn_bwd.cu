@@ -26,13 +26,24 @@ cudaError_t run_bwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMa
       (e = cudaFuncSetAttribute(kdq, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytesDQ)) !=
           cudaSuccess)
     return e;
+  // Causal order: groups of heads whose streamed tiles (Q and dO of all the
+  // query heads of a KV head for dK/dV; K and V for dQ) take at most 48 MiB.
+  const long long per_head = 4LL * base.N * 128;
+  auto group_of = [&](long long bytes, int heads) {
+    long long hg = (48LL << 20) / (bytes > 0 ? bytes : 1);
+    return static_cast<int>(hg < 1 ? 1 : (hg > heads ? heads : hg));
+  };
   BwdParams p1 = base;
   p1.num_units = base.BHk * base.nb;
+  p1.hgroup = group_of(per_head * base.group, base.BHk);
+  if ((e = unit_counter(stream, &p1.sched)) != cudaSuccess) return e;
   const int g1 = p1.num_units < sms ? p1.num_units : sms;
   kdkdv<<<g1, C::kThreads, C::kSmemBytes, stream>>>(q, k, v, dO, p1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   BwdParams p2 = base;
   p2.num_units = base.BH * base.nb;
+  p2.hgroup = group_of(per_head, base.BH);
+  if ((e = unit_counter(stream, &p2.sched)) != cudaSuccess) return e;
   const int g2 = p2.num_units < sms ? p2.num_units : sms;
   kdq<<<g2, C::kThreads, C::kSmemBytesDQ, stream>>>(q, k, v, dO, p2);
   return cudaGetLastError();

@@ -55,6 +55,8 @@ struct BwdParams {
   int window, causal;
   int nb;                // ceil(N / 128): query blocks == key blocks
   int num_units;
+  int hgroup;            // causal order: heads per group (their streamed tiles stay in L2)
+  int* sched;            // unit counter for dynamic scheduling (zeroed before launch), or null
   float scale_log2;      // scale * log2(e)
   float scale;
   unsigned long long timeout_ns;
@@ -101,9 +103,27 @@ struct BwdCtl {
   uint64_t ds_ready;       // dK/dV: dS^T written (16 warp arrivals)
   uint64_t unit_done;      // the unit's accumulators final
   uint64_t drain;
+  uint64_t unit_full[4];   // ring of work-unit indices handed out by the load warp
+  uint64_t unit_empty[4];
+  int unit_ring[4];
   uint32_t tmem_base;
   int abort_flag;
 };
+
+// Causal unit order shared by both kernels: longest first within groups of
+// `hgroup` heads (bigger first when `ascending` is false), the groups one after
+// the other.  Returns (head, block).
+__device__ __forceinline__ void bwd_causal_order(int u, int heads, int nb, int hgroup, bool ascending,
+                                                 int& head, int& blk) {
+  const int HG = hgroup > 0 ? min(hgroup, heads) : heads;
+  const int per_group = HG * nb;
+  const int g = u / per_group;
+  const int v = u - g * per_group;
+  const int hg = min(HG, heads - g * HG);
+  const int rr = v / hg;
+  head = g * HG + (v - rr * hg);
+  blk = ascending ? rr : nb - 1 - rr;
+}
 
 // Query blocks [i_lo, i_hi] that see key block j.
 __device__ __forceinline__ void bwd_qrange(int j, const BwdParams& p, int& i_lo, int& i_hi) {
@@ -159,6 +179,10 @@ __global__ void __launch_bounds__(576, 1)
     mbar_init(bar(ctl.ds_ready), C::kEW);
     mbar_init(bar(ctl.unit_done), 1);
     mbar_init(bar(ctl.drain), 1);
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(bar(ctl.unit_full[s]), 1);
+      mbar_init(bar(ctl.unit_empty[s]), C::kEW + 1);   // the MMA thread and the element-wise warps
+    }
     ctl.abort_flag = 0;
     fence_mbarrier_init();
     fence_proxy_async_smem();
@@ -172,13 +196,33 @@ __global__ void __launch_bounds__(576, 1)
   tc_fence_after();
   const uint32_t tmem = ctl.tmem_base;
   const WaitCtx wc{&ctl.abort_flag, p.status ? p.status : &g_attn_status, p.timeout_ns};
+  // Work units: the load warp takes the next index (atomic counter, or the
+  // static stride without one) and passes it through a 4-entry ring; -1 ends.
+  auto publish_unit = [&](uint32_t k, bool& ok) -> int {
+    int u = p.sched ? atomicAdd(p.sched, 1) : static_cast<int>(blockIdx.x + k * gridDim.x);
+    if (u >= p.num_units) u = -1;
+    const uint32_t slot = k & 3;
+    if (k >= 4 && !(ok = wait_bounded(bar(ctl.unit_empty[slot]), ((k >> 2) - 1) & 1, wc))) return -1;
+    ctl.unit_ring[slot] = u;
+    mbar_arrive(bar(ctl.unit_full[slot]));
+    return u;
+  };
+  auto take_unit = [&](uint32_t k, bool& ok, bool single) -> int {
+    const uint32_t slot = k & 3;
+    ok = wait_bounded(bar(ctl.unit_full[slot]), (k >> 2) & 1, wc);
+    if (!single) ok = __all_sync(0xffffffffu, ok);
+    if (!ok) return -1;
+    const int u = *reinterpret_cast<volatile int*>(&ctl.unit_ring[slot]);
+    if (!single) __syncwarp();
+    if (single || lane == 0) mbar_arrive(bar(ctl.unit_empty[slot]));
+    return u;
+  };
 
   // Unit u -> (bhk, j).  Causal: ascending j (key block 0 sees the most query
   // blocks) across all heads first; otherwise the key blocks of one head in turn.
   auto unit = [&](int u, int& bhk, int& j) {
     if (p.causal) {
-      j = u / p.BHk;
-      bhk = u - j * p.BHk;
+      bwd_causal_order(u, p.BHk, p.nb, p.hgroup, true, bhk, j);   // key block 0 sees the most
     } else {
       bhk = u / p.nb;
       j = u - bhk * p.nb;
@@ -196,7 +240,9 @@ __global__ void __launch_bounds__(576, 1)
       const uint64_t pol_ring = l2_policy_evict_last();
       uint32_t item = 0, uit = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uit) {
+      for (uint32_t k = 0; ok; ++k, ++uit) {
+        const int u = publish_unit(k, ok);
+        if (u < 0) break;
         int bhk, j;
         unit(u, bhk, j);
         int i_lo, i_hi;
@@ -262,7 +308,9 @@ __global__ void __launch_bounds__(576, 1)
                      C::kIdescTS, (acc || k > 0) ? 1u : 0u);
         }
       };
-      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uit) {
+      for (uint32_t k = 0; ok; ++k, ++uit) {
+        const int u = take_unit(k, ok, true);
+        if (u < 0) break;
         int bhk, j;
         unit(u, bhk, j);
         int i_lo, i_hi;
@@ -323,7 +371,9 @@ __global__ void __launch_bounds__(576, 1)
     const float cl = p.scale_log2;
     uint32_t uit = 0, gblk = 0, item = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uit) {
+    for (uint32_t k = 0; ok; ++k, ++uit) {
+      const int u = take_unit(k, ok, false);
+      if (u < 0) break;
       int bhk, j;
       unit(u, bhk, j);
       int i_lo, i_hi;
@@ -497,6 +547,10 @@ __global__ void __launch_bounds__(576, 1)
     mbar_init(bar(ctl.p_ready), C::kEW);    // dS written
     mbar_init(bar(ctl.unit_done), 1);
     mbar_init(bar(ctl.drain), 1);
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(bar(ctl.unit_full[s]), 1);
+      mbar_init(bar(ctl.unit_empty[s]), C::kEW + 1);   // the MMA thread and the element-wise warps
+    }
     ctl.abort_flag = 0;
     fence_mbarrier_init();
     fence_proxy_async_smem();
@@ -510,13 +564,32 @@ __global__ void __launch_bounds__(576, 1)
   tc_fence_after();
   const uint32_t tmem = ctl.tmem_base;
   const WaitCtx wc{&ctl.abort_flag, p.status ? p.status : &g_attn_status, p.timeout_ns};
+  // Work units: the load warp takes the next index (atomic counter, or the
+  // static stride without one) and passes it through a 4-entry ring; -1 ends.
+  auto publish_unit = [&](uint32_t k, bool& ok) -> int {
+    int u = p.sched ? atomicAdd(p.sched, 1) : static_cast<int>(blockIdx.x + k * gridDim.x);
+    if (u >= p.num_units) u = -1;
+    const uint32_t slot = k & 3;
+    if (k >= 4 && !(ok = wait_bounded(bar(ctl.unit_empty[slot]), ((k >> 2) - 1) & 1, wc))) return -1;
+    ctl.unit_ring[slot] = u;
+    mbar_arrive(bar(ctl.unit_full[slot]));
+    return u;
+  };
+  auto take_unit = [&](uint32_t k, bool& ok, bool single) -> int {
+    const uint32_t slot = k & 3;
+    ok = wait_bounded(bar(ctl.unit_full[slot]), (k >> 2) & 1, wc);
+    if (!single) ok = __all_sync(0xffffffffu, ok);
+    if (!ok) return -1;
+    const int u = *reinterpret_cast<volatile int*>(&ctl.unit_ring[slot]);
+    if (!single) __syncwarp();
+    if (single || lane == 0) mbar_arrive(bar(ctl.unit_empty[slot]));
+    return u;
+  };
 
   // Unit u -> (bh, i).  Causal: longest first (last query blocks of all heads).
   auto unit = [&](int u, int& bh, int& i) {
     if (p.causal) {
-      const int rr = u / p.BH;
-      bh = u - rr * p.BH;
-      i = p.nb - 1 - rr;
+      bwd_causal_order(u, p.BH, p.nb, p.hgroup, false, bh, i);    // the last query block sees the most
     } else {
       bh = u / p.nb;
       i = u - bh * p.nb;
@@ -535,7 +608,9 @@ __global__ void __launch_bounds__(576, 1)
       const uint64_t pol_ring = l2_policy_evict_last();
       uint32_t item = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+      for (uint32_t k = 0; ok; ++k) {
+        const int u = publish_unit(k, ok);
+        if (u < 0) break;
         int bh, i;
         unit(u, bh, i);
         int j_lo, j_hi;
@@ -576,7 +651,9 @@ __global__ void __launch_bounds__(576, 1)
                      C::kIdescSS, k > 0 ? 1u : 0u);
         }
       };
-      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uit) {
+      for (uint32_t k = 0; ok; ++k, ++uit) {
+        const int u = take_unit(k, ok, true);
+        if (u < 0) break;
         int bh, i;
         unit(u, bh, i);
         int j_lo, j_hi;
@@ -636,7 +713,9 @@ __global__ void __launch_bounds__(576, 1)
     const float cl = p.scale_log2;
     uint32_t uit = 0, gblk = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uit) {
+    for (uint32_t k = 0; ok; ++k, ++uit) {
+      const int u = take_unit(k, ok, false);
+      if (u < 0) break;
       int bh, i;
       unit(u, bh, i);
       int j_lo, j_hi;
