@@ -327,7 +327,9 @@ def run_mine(args):
     e2e_steps(2)
     torch.cuda.synchronize(dev)
     barrier()
-    n_e2e = max(3, args.steps // 2)
+    # Enough steps that filling and draining the three-stage pipeline (about one
+    # step's latency) is a small part of the timed interval.
+    n_e2e = max(20, args.steps)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(s_up)
@@ -489,7 +491,7 @@ def run_mine(args):
                          "traffic": traffic, "peak_source": peaks["source"] + " bf16 burst"},
             "e2e": {"value": w.flops / (ms_e2e * 1e-3) / 1e12 * ws, "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e,
-                    "pipelined": "2 buffer sets, upload/compute/download streams"},
+                    "steps": n_e2e, "pipelined": "2 buffer sets, upload/compute/download streams"},
             "gpu_launches": args.steps,
             "clocks": {k2: clocks[k2] for k2 in ("sm_mhz", "sm_max_mhz", "reasons")},
             "cpu_baseline": cpu,

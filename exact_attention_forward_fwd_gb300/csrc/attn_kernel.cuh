@@ -20,7 +20,8 @@
 //   * warps 0-3 / 4-7: softmax of tile 0 / tile 1, one thread per query row,
 //     reading S from tensor memory (TMEM) and writing P back over it;
 //   * warp 8: TMA loads of Q (once per unit) and of K, V blocks into the ring;
-//   * warp 9: allocates TMEM and issues every tcgen05.mma from one thread:
+//   * warp 9: allocates TMEM and issues every tcgen05.mma (the warp runs its
+//     loop converged, one elected lane issues):
 //       S_t = Q_t K_j^T  (SS, both operands K-major in shared memory)
 //       O_t += P_t V_j   (TS, P from TMEM, V from shared memory)
 //     ordered PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), ... so the tensor pipe
@@ -238,7 +239,7 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(bar(ctl.drain), 1);
     for (int s = 0; s < 4; ++s) {
       mbar_init(bar(ctl.unit_full[s]), 1);
-      mbar_init(bar(ctl.unit_empty[s]), 9);   // the MMA thread and the 8 softmax warps
+      mbar_init(bar(ctl.unit_empty[s]), 9);   // the MMA warp and the 8 softmax warps
     }
     ctl.abort_flag = 0;
     fence_mbarrier_init();
@@ -265,15 +266,15 @@ __global__ void __launch_bounds__(320, 1)
     mbar_arrive(bar(ctl.unit_full[slot]));
     return u;
   };
-  // Consumer side (whole warp, or the MMA thread alone with `single`).
-  auto take_unit = [&](uint32_t k, bool& ok, bool single) -> int {
+  // Consumer side (a whole warp; lane 0 frees the slot).
+  auto take_unit = [&](uint32_t k, bool& ok) -> int {
     const uint32_t slot = k & 3;
     ok = wait_bounded(bar(ctl.unit_full[slot]), (k >> 2) & 1, wc);
-    if (!single) ok = __all_sync(0xffffffffu, ok);
+    ok = __all_sync(0xffffffffu, ok);
     if (!ok) return -1;
     const int u = *reinterpret_cast<volatile int*>(&ctl.unit_ring[slot]);
-    if (!single) __syncwarp();
-    if (single || lane == 0) mbar_arrive(bar(ctl.unit_empty[slot]));
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(ctl.unit_empty[slot]));
     return u;
   };
 
@@ -343,9 +344,14 @@ __global__ void __launch_bounds__(320, 1)
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs this loop converged; each MMA and commit is issued by
+    // one elected lane (the *_w forms), every wait is taken by all lanes.
+    {
       uint32_t item = 0, uit = 0, pr[2] = {0, 0};
       bool ok = true;
+      auto wait_w = [&](uint64_t& b, uint32_t parity) {
+        return __all_sync(0xffffffffu, wait_bounded(bar(b), parity, wc));
+      };
       auto s_mma = [&](int t, uint32_t kslot) {
         const uint32_t a0 = sQ + t * C::kTileBytes;
         const uint32_t b0 = sKV + kslot * C::kTileBytes;
@@ -355,9 +361,9 @@ __global__ void __launch_bounds__(320, 1)
           const uint64_t da = make_smem_desc(a0 + off, 16, 1024, kSwizzle128B);
           const uint64_t db = make_smem_desc(b0 + off, 16, 1024, kSwizzle128B);
           if (FP8)
-            mma_f8_ss(tmem + 128 * t, da, db, C::kIdescS, k > 0);
+            mma_f8_ss_w(tmem + 128 * t, da, db, C::kIdescS, k > 0);
           else
-            mma_f16_ss(tmem + 128 * t, da, db, C::kIdescS, k > 0);
+            mma_f16_ss_w(tmem + 128 * t, da, db, C::kIdescS, k > 0);
         }
       };
       // O_t += P_t V over the keys of half `hf` of the block (P of each half is
@@ -370,77 +376,77 @@ __global__ void __launch_bounds__(320, 1)
           const uint32_t a = tmem + 128 * t + k * 8;
           if (FP8) {
             const uint64_t db = make_smem_desc(b0 + k * 32, 16, 1024, kSwizzle128B);
-            mma_f8_ts(tmem + 256 + D * t, a, db, C::kIdescPV, (acc || k > 0) ? 1u : 0u);
+            mma_f8_ts_w(tmem + 256 + D * t, a, db, C::kIdescPV, (acc || k > 0) ? 1u : 0u);
           } else {
             const uint64_t db = make_smem_desc(b0 + k * 2048, 16384, 1024, kSwizzle128B);
-            mma_f16_ts(tmem + 256 + D * t, a, db, C::kIdescPV, (acc || k > 0) ? 1u : 0u);
+            mma_f16_ts_w(tmem + 256 + D * t, a, db, C::kIdescPV, (acc || k > 0) ? 1u : 0u);
           }
         }
       };
       auto wait_item = [&](uint32_t it) {
-        return wait_bounded(bar(ctl.kv_full[it % C::kStages]), (it / C::kStages) & 1, wc);
+        return wait_w(ctl.kv_full[it % C::kStages], (it / C::kStages) & 1);
       };
       for (uint32_t k = 0; ok; ++k) {
-        const int u = take_unit(k, ok, true);
+        const int u = take_unit(k, ok);
         if (u < 0) break;
         const Unit w = unit_of(u, p);
         const int J = w.nblocks;
         if (J == 0) continue;   // empty key range (split-KV)
-        ok = wait_bounded(bar(ctl.q_full[0]), uit & 1, wc) &&
-             wait_bounded(bar(ctl.q_full[1]), uit & 1, wc);
+        ok = wait_w(ctl.q_full[0], uit & 1) && wait_w(ctl.q_full[1], uit & 1);
         if (!ok) break;
         const uint32_t base = item;            // K_j = base + 2j, V_j = base + 2j + 1
         item += 2 * J;
         if (!(ok = wait_item(base))) break;
         tc_fence_after();
         s_mma(0, base % C::kStages);
-        mma_commit(bar(ctl.s_full[0]));
+        mma_commit_w(bar(ctl.s_full[0]));
         s_mma(1, base % C::kStages);
-        mma_commit(bar(ctl.s_full[1]));
-        mma_commit(bar(ctl.kv_empty[base % C::kStages]));
+        mma_commit_w(bar(ctl.s_full[1]));
+        mma_commit_w(bar(ctl.kv_empty[base % C::kStages]));
         if (J == 1) {
-          mma_commit(bar(ctl.q_empty[0]));
-          mma_commit(bar(ctl.q_empty[1]));
+          mma_commit_w(bar(ctl.q_empty[0]));
+          mma_commit_w(bar(ctl.q_empty[1]));
         }
         for (int j = 0; j < J && ok; ++j) {
           const uint32_t iv = base + 2 * j + 1, ik = base + 2 * j + 2;
           const uint32_t vslot = iv % C::kStages, kslot = ik % C::kStages;
           if (!(ok = wait_item(iv))) break;
-          if (!(ok = wait_bounded(bar(ctl.p_ready[0][0]), pr[0] & 1, wc))) break;
+          if (!(ok = wait_w(ctl.p_ready[0][0], pr[0] & 1))) break;
           tc_fence_after();
           pv_mma(0, vslot, j > 0, 0);
-          if (!(ok = wait_bounded(bar(ctl.p_ready[0][1]), pr[0]++ & 1, wc))) break;
+          if (!(ok = wait_w(ctl.p_ready[0][1], pr[0]++ & 1))) break;
           tc_fence_after();
           pv_mma(0, vslot, j > 0, 1);
-          if (j == J - 1) mma_commit(bar(ctl.o_final[0]));
+          if (j == J - 1) mma_commit_w(bar(ctl.o_final[0]));
           if (j + 1 < J) {
             if (!(ok = wait_item(ik))) break;
             tc_fence_after();
             s_mma(0, kslot);
-            mma_commit(bar(ctl.s_full[0]));
+            mma_commit_w(bar(ctl.s_full[0]));
           }
-          if (!(ok = wait_bounded(bar(ctl.p_ready[1][0]), pr[1] & 1, wc))) break;
+          if (!(ok = wait_w(ctl.p_ready[1][0], pr[1] & 1))) break;
           tc_fence_after();
           pv_mma(1, vslot, j > 0, 0);
-          if (!(ok = wait_bounded(bar(ctl.p_ready[1][1]), pr[1]++ & 1, wc))) break;
+          if (!(ok = wait_w(ctl.p_ready[1][1], pr[1]++ & 1))) break;
           tc_fence_after();
           pv_mma(1, vslot, j > 0, 1);
-          mma_commit(bar(ctl.kv_empty[vslot]));
-          if (j == J - 1) mma_commit(bar(ctl.o_final[1]));
+          mma_commit_w(bar(ctl.kv_empty[vslot]));
+          if (j == J - 1) mma_commit_w(bar(ctl.o_final[1]));
           if (j + 1 < J) {
             s_mma(1, kslot);
-            mma_commit(bar(ctl.s_full[1]));
-            mma_commit(bar(ctl.kv_empty[kslot]));
+            mma_commit_w(bar(ctl.s_full[1]));
+            mma_commit_w(bar(ctl.kv_empty[kslot]));
             if (j + 2 == J) {
-              mma_commit(bar(ctl.q_empty[0]));
-              mma_commit(bar(ctl.q_empty[1]));
+              mma_commit_w(bar(ctl.q_empty[0]));
+              mma_commit_w(bar(ctl.q_empty[1]));
             }
           }
         }
         ++uit;
       }
       // Every MMA issued must finish before TMEM is released.
-      mma_commit(bar(ctl.drain));
+      __syncwarp();
+      mma_commit_w(bar(ctl.drain));
       wait_bounded(bar(ctl.drain), 0, wc, false);
     }
   } else {
@@ -456,7 +462,7 @@ __global__ void __launch_bounds__(320, 1)
     uint32_t sit = 0, uit = 0;
     bool ok = true;
     for (uint32_t k = 0; ok; ++k) {
-      const int u = take_unit(k, ok, false);
+      const int u = take_unit(k, ok);
       if (u < 0) break;
       const Unit w = unit_of(u, p);
       const int row = w.pair * 256 + t * 128 + r;
