@@ -33,7 +33,11 @@
 //   * conditional rescaling: the reference max used for the exponentials is
 //     only moved (and O~, l rescaled) when the block max exceeds it by more
 //     than tau (base-2 units).  Numerator and denominator always share the
-//     same reference, so the result stays exact; p <= 2^tau.
+//     same reference, so the result stays exact; p <= 2^tau.  The bf16 path
+//     takes the exponentials against the current reference and the block max
+//     in one pass, and takes the block again in the rare case the max moved
+//     by more than tau (S is still in TMEM then), so no exponential waits
+//     for a row max.
 //   * because every tcgen05.commit tracks all earlier MMAs of the issuing
 //     thread, the arrival of S_t(j) also proves O_t += P_t(j-1) V(j-1) is
 //     complete: a rescale of O~ right after waiting for S_t(j) is race-free.
@@ -497,16 +501,6 @@ __global__ void __launch_bounds__(320, 1)
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
-        uint32_t sr[128];
-        tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-        tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-        tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
-        tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
-        tmem_wait_ld();
-        reg_fence(sr);
-        float x[128];
-#pragma unroll
-        for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(sr[c]);
         float cj = p.scale_log2;
         float v_fold = 1.0f;
         if (FP8) {
@@ -515,24 +509,35 @@ __global__ void __launch_bounds__(320, 1)
         }
         const int lim = lim_row - j * 128;    // columns > lim are invisible
         const int lo = lo_row - j * 128;      // columns < lo are invisible (window)
-        if (lim < 127 || lo > 0) {
+        // S of this block -> x (raw scores; invisible columns -inf).
+        auto load_s = [&](float (&x)[128]) {
+          uint32_t sr[128];
+          tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+          tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+          tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
+          tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
+          tmem_wait_ld();
+          reg_fence(sr);
 #pragma unroll
-          for (int c = 0; c < 128; ++c) x[c] = (c > lim || c < lo) ? NEG_INF : x[c];
-        }
-        float m0 = x[0], m1 = x[1], m2 = x[2], m3 = x[3];
+          for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(sr[c]);
+          if (lim < 127 || lo > 0) {
 #pragma unroll
-        for (int c = 4; c < 128; c += 8) {
-          m0 = max3(m0, x[c], x[c + 1]);
-          m1 = max3(m1, x[c + 2], x[c + 3]);
-          m2 = max3(m2, x[c + 4], x[c + 5]);
-          m3 = max3(m3, x[c + 6], x[c + 7]);
-        }
-        const float mx = max3(m0, m1, fmaxf(m2, m3));
-        const float m_blk = mx * cj;
-        const bool need = m_blk > m_ref + tau;
-        const float m_new = need ? m_blk : m_ref;
-        const float alpha = need ? ex2_approx(m_ref - m_new) : 1.0f;   // 0 when m_ref = -inf
-        if (jj > 0 && __any_sync(0xffffffffu, need)) {
+            for (int c = 0; c < 128; ++c) x[c] = (c > lim || c < lo) ? NEG_INF : x[c];
+          }
+        };
+        auto row_max = [&](const float (&x)[128]) {
+          float m0 = x[0], m1 = x[1], m2 = x[2], m3 = x[3];
+#pragma unroll
+          for (int c = 4; c < 128; c += 8) {
+            m0 = max3(m0, x[c], x[c + 1]);
+            m1 = max3(m1, x[c + 2], x[c + 3]);
+            m2 = max3(m2, x[c + 4], x[c + 5]);
+            m3 = max3(m3, x[c + 6], x[c + 7]);
+          }
+          return max3(m0, m1, fmaxf(m2, m3));
+        };
+        // O_t *= alpha (per row); only called when some row of the warp needs it.
+        auto rescale_o = [&](float alpha) {
 #pragma unroll 1
           for (int cc = 0; cc < D; cc += 32) {
             uint32_t orow[32];
@@ -543,13 +548,21 @@ __global__ void __launch_bounds__(320, 1)
             for (int i = 0; i < 32; ++i) orow[i] = __float_as_uint(__uint_as_float(orow[i]) * alpha);
             tmem_st32(tO + cc, orow);
           }
-        }
-        ell *= alpha;
-        ell_r *= alpha;
-        m_ref = m_new;
-        const float m_use = (m_ref == NEG_INF) ? 0.0f : m_ref;
-        __syncwarp();   // tcgen05.st is warp-collective: reconverge after the mask branch
-        if (FP8) {
+        };
+        if constexpr (FP8) {
+          // FP8 P must stay within E4M3's range, so the block max is taken first
+          // and the reference follows it exactly (tau = 0).
+          float x[128];
+          load_s(x);
+          const float m_blk = row_max(x) * cj;
+          const bool need = m_blk > m_ref + tau;
+          const float m_new = need ? m_blk : m_ref;
+          const float alpha = need ? ex2_approx(m_ref - m_new) : 1.0f;   // 0 when m_ref = -inf
+          if (jj > 0 && __any_sync(0xffffffffu, need)) rescale_o(alpha);
+          ell *= alpha;
+          m_ref = m_new;
+          const float m_use = (m_ref == NEG_INF) ? 0.0f : m_ref;
+          __syncwarp();   // tcgen05.st is warp-collective: reconverge after the mask branch
           // p' = p * v_fold = 2^(s c - (m - log2 v_fold)): V's block scale rides in
           // the exponent, and the block's sum of p is sum(p') / v_fold.
           const float m_f = m_use - __log2f(v_fold);
@@ -581,33 +594,75 @@ __global__ void __launch_bounds__(320, 1)
           f32x2_unpack(f32x2_add(s01, s23), a0, a1);
           ell += (a0 + a1) / v_fold;
         } else {
-          // p = 2^(s*c - m) in pairs.  P is rounded to bf16 for the PV MMA; the
+          // p = 2^(s*c - m) against the running reference max m, with the block's
+          // own max taken in the same pass, so no exponential waits for a max.
+          // The pass stands unless the block's max rose more than tau above m
+          // (rare after the first block); then m moves to the block's max, O and
+          // the sums are rescaled and the block (still in TMEM: P has not been
+          // stored yet) is taken again.  P is rounded to bf16 for the PV MMA; the
           // sum of exactly those rounded values (l~) normalises O, so numerator
-          // and denominator use the same weights, while the sum of the f32
-          // values (l) gives the logsumexp.
-          const uint64_t c2 = f32x2_pack(cj, cj);
-          const uint64_t nm2 = f32x2_pack(-m_use, -m_use);
-          uint64_t ex0 = 0, ex1 = 0;   // (0.f, 0.f)
-          float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
+          // and denominator use the same weights, while the sum of the f32 values
+          // (l) gives the logsumexp.
           uint32_t pk[64];
-#pragma unroll
-          for (int i = 0; i < 64; ++i) {
-            float t0, t1;
-            f32x2_unpack(f32x2_fma(f32x2_pack(x[2 * i], x[2 * i + 1]), c2, nm2), t0, t1);
-            const float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
-            const uint32_t pb = pack_bf16x2(p0, p1);
-            pk[i] = pb;
-            const uint64_t e = f32x2_pack(p0, p1);
-            if (i & 1) {
-              r2 = add_bf16_lo(pb, r2);
-              r3 = add_bf16_hi(pb, r3);
-              ex1 = f32x2_add(ex1, e);
-            } else {
-              r0 = add_bf16_lo(pb, r0);
-              r1 = add_bf16_hi(pb, r1);
-              ex0 = f32x2_add(ex0, e);
+          float e_sum, r_sum;
+          // A row that has seen no visible key yet (every row at a unit's first
+          // block) takes its reference from this block's max before the pass;
+          // its O and sums are still 0, so nothing is rescaled.
+          bool pre = !__all_sync(0xffffffffu, m_ref != NEG_INF);
+          for (;;) {
+            float x[128];
+            load_s(x);
+            if (pre) {
+              const float m_blk0 = row_max(x) * cj;
+              if (m_ref == NEG_INF) m_ref = m_blk0;
+              pre = false;
             }
+            const float m_use = (m_ref == NEG_INF) ? 0.0f : m_ref;
+            const uint64_t c2 = f32x2_pack(cj, cj);
+            const uint64_t nm2 = f32x2_pack(-m_use, -m_use);
+            uint64_t ex0 = 0, ex1 = 0;   // (0.f, 0.f)
+            float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
+            float m0 = NEG_INF, m1 = NEG_INF, m2 = NEG_INF, m3 = NEG_INF;
+#pragma unroll
+            for (int i = 0; i < 64; ++i) {
+              float t0, t1;
+              f32x2_unpack(f32x2_fma(f32x2_pack(x[2 * i], x[2 * i + 1]), c2, nm2), t0, t1);
+              const float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
+              const uint32_t pb = pack_bf16x2(p0, p1);
+              pk[i] = pb;
+              const uint64_t e = f32x2_pack(p0, p1);
+              switch (i & 3) {
+                case 0: m0 = max3(m0, x[2 * i], x[2 * i + 1]); break;
+                case 1: m1 = max3(m1, x[2 * i], x[2 * i + 1]); break;
+                case 2: m2 = max3(m2, x[2 * i], x[2 * i + 1]); break;
+                default: m3 = max3(m3, x[2 * i], x[2 * i + 1]); break;
+              }
+              if (i & 1) {
+                r2 = add_bf16_lo(pb, r2);
+                r3 = add_bf16_hi(pb, r3);
+                ex1 = f32x2_add(ex1, e);
+              } else {
+                r0 = add_bf16_lo(pb, r0);
+                r1 = add_bf16_hi(pb, r1);
+                ex0 = f32x2_add(ex0, e);
+              }
+            }
+            const float m_blk = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)) * cj;
+            const bool need = m_blk > m_ref + tau;
+            if (!__any_sync(0xffffffffu, need)) {
+              float b0, b1;
+              f32x2_unpack(f32x2_add(ex0, ex1), b0, b1);
+              e_sum = b0 + b1;
+              r_sum = (r0 + r1) + (r2 + r3);
+              break;
+            }
+            const float alpha = need ? ex2_approx(m_ref - m_blk) : 1.0f;
+            if (jj > 0) rescale_o(alpha);
+            ell *= alpha;
+            ell_r *= alpha;
+            if (need) m_ref = m_blk;
           }
+          __syncwarp();   // tcgen05.st is warp-collective
           tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
           tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
           // bf16: one signal for both halves of the keys (a half's PV is as long
@@ -616,10 +671,8 @@ __global__ void __launch_bounds__(320, 1)
           tc_fence_before();
           mbar_arrive(bar(ctl.p_ready[t][0]));
           mbar_arrive(bar(ctl.p_ready[t][1]));
-          float b0, b1;
-          f32x2_unpack(f32x2_add(ex0, ex1), b0, b1);
-          ell_r += (r0 + r1) + (r2 + r3);
-          ell += b0 + b1;
+          ell_r += r_sum;
+          ell += e_sum;
         }
       }
       if (!ok) break;
