@@ -207,14 +207,14 @@ __global__ void __launch_bounds__(576, 1)
     mbar_arrive(bar(ctl.unit_full[slot]));
     return u;
   };
-  auto take_unit = [&](uint32_t k, bool& ok, bool single) -> int {
+  auto take_unit = [&](uint32_t k, bool& ok) -> int {   // a whole warp; lane 0 frees the slot
     const uint32_t slot = k & 3;
     ok = wait_bounded(bar(ctl.unit_full[slot]), (k >> 2) & 1, wc);
-    if (!single) ok = __all_sync(0xffffffffu, ok);
+    ok = __all_sync(0xffffffffu, ok);
     if (!ok) return -1;
     const int u = *reinterpret_cast<volatile int*>(&ctl.unit_ring[slot]);
-    if (!single) __syncwarp();
-    if (single || lane == 0) mbar_arrive(bar(ctl.unit_empty[slot]));
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(ctl.unit_empty[slot]));
     return u;
   };
 
@@ -283,19 +283,24 @@ __global__ void __launch_bounds__(576, 1)
     }
   } else if (warp == C::kEW + 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs this loop converged; one elected lane issues each
+    // MMA and commit (the *_w forms), every wait is taken by all lanes.
+    {
       uint32_t item = 0, uit = 0, gblk = 0;
+      auto wait_w = [&](uint32_t b, uint32_t parity) {
+        return __all_sync(0xffffffffu, wait_bounded(b, parity, wc));
+      };
       bool ok = true;
       auto wait_slot = [&](uint32_t it) {
-        return wait_bounded(bar(ctl.full[it % C::kStages]), (it / C::kStages) & 1, wc);
+        return wait_w(bar(ctl.full[it % C::kStages]), (it / C::kStages) & 1);
       };
       // SS product [M = 128 rows of a] x [N = 128 rows of b]^T over K = D.
       auto ss = [&](uint32_t d_col, uint32_t a0, uint32_t b0) {
 #pragma unroll
         for (int k = 0; k < C::kSSteps; ++k) {
           const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-          mma_f16_ss(tmem + d_col, make_smem_desc(a0 + off, 16, 1024, kSwizzle128B),
-                     make_smem_desc(b0 + off, 16, 1024, kSwizzle128B), C::kIdescSS, k > 0);
+          mma_f16_ss_w(tmem + d_col, make_smem_desc(a0 + off, 16, 1024, kSwizzle128B),
+                       make_smem_desc(b0 + off, 16, 1024, kSwizzle128B), C::kIdescSS, k > 0);
         }
       };
       // TS product: A = 128 x 128 bf16 in TMEM, queries [32h, 32h+32) at
@@ -304,19 +309,19 @@ __global__ void __launch_bounds__(576, 1)
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint32_t a = tmem + a_col + (k >> 1) * 32 + (k & 1) * 8;
-          mma_f16_ts(tmem + d_col, a, make_smem_desc(b0 + k * 2048, 16384, 1024, kSwizzle128B),
-                     C::kIdescTS, (acc || k > 0) ? 1u : 0u);
+          mma_f16_ts_w(tmem + d_col, a, make_smem_desc(b0 + k * 2048, 16384, 1024, kSwizzle128B),
+                       C::kIdescTS, (acc || k > 0) ? 1u : 0u);
         }
       };
       for (uint32_t k = 0; ok; ++k, ++uit) {
-        const int u = take_unit(k, ok, true);
+        const int u = take_unit(k, ok);
         if (u < 0) break;
         int bhk, j;
         unit(u, bhk, j);
         int i_lo, i_hi;
         bwd_qrange(j, p, i_lo, i_hi);
         const int T = p.group * (i_hi - i_lo + 1);
-        if (!(ok = wait_bounded(bar(ctl.fix_full), uit & 1, wc))) break;
+        if (!(ok = wait_w(bar(ctl.fix_full), uit & 1))) break;
         // Block t: Q item = base + 2t, dO item = base + 2t + 1.
         const uint32_t base = item;
         item += 2 * T;
@@ -324,42 +329,43 @@ __global__ void __launch_bounds__(576, 1)
         if (!(ok = wait_slot(base) && wait_slot(base + 1))) break;
         tc_fence_after();
         ss(0, sK, sRing + (base % C::kStages) * C::kTile);
-        mma_commit(bar(ctl.s_full));
+        mma_commit_w(bar(ctl.s_full));
         ss(128, sV, sRing + ((base + 1) % C::kStages) * C::kTile);
-        mma_commit(bar(ctl.dp_full));
+        mma_commit_w(bar(ctl.dp_full));
         for (int t = 0; t < T && ok; ++t, ++gblk) {
           const uint32_t iq = base + 2 * t, io = iq + 1;
           const uint32_t sQ = sRing + (iq % C::kStages) * C::kTile;
           const uint32_t sdO = sRing + (io % C::kStages) * C::kTile;
           // dV += P^T dO once P^T is written
-          if (!(ok = wait_bounded(bar(ctl.p_ready), gblk & 1, wc))) break;
+          if (!(ok = wait_w(bar(ctl.p_ready), gblk & 1))) break;
           tc_fence_after();
           ts(256, 0, sdO, t > 0);
-          mma_commit(bar(ctl.empty[io % C::kStages]));    // dO_i done (dP^T(t) was earlier)
+          mma_commit_w(bar(ctl.empty[io % C::kStages]));    // dO_i done (dP^T(t) was earlier)
           // S^T(t+1): the S^T columns are free once dV(t) has read P^T
           const bool more = t + 1 < T;
           if (more) {
             if (!(ok = wait_slot(iq + 2))) break;
             tc_fence_after();
             ss(0, sK, sRing + ((iq + 2) % C::kStages) * C::kTile);
-            mma_commit(bar(ctl.s_full));   // P^T(t+1) can start during dK(t), dP^T(t+1)
+            mma_commit_w(bar(ctl.s_full));   // P^T(t+1) can start during dK(t), dP^T(t+1)
           }
           // dK += dS^T Q once dS^T is written
-          if (!(ok = wait_bounded(bar(ctl.ds_ready), gblk & 1, wc))) break;
+          if (!(ok = wait_w(bar(ctl.ds_ready), gblk & 1))) break;
           tc_fence_after();
           ts(256 + D, 128, sQ, t > 0);
-          mma_commit(bar(ctl.empty[iq % C::kStages]));    // Q_i done
+          mma_commit_w(bar(ctl.empty[iq % C::kStages]));    // Q_i done
           if (more) {
             if (!(ok = wait_slot(io + 2))) break;
             tc_fence_after();
             ss(128, sV, sRing + ((io + 2) % C::kStages) * C::kTile);
-            mma_commit(bar(ctl.dp_full));
+            mma_commit_w(bar(ctl.dp_full));
           }
         }
-        mma_commit(bar(ctl.unit_done));
-        mma_commit(bar(ctl.fix_empty));
+        mma_commit_w(bar(ctl.unit_done));
+        mma_commit_w(bar(ctl.fix_empty));
       }
-      mma_commit(bar(ctl.drain));
+      __syncwarp();
+      mma_commit_w(bar(ctl.drain));
       wait_bounded(bar(ctl.drain), 0, wc, false);
     }
   } else {
@@ -372,7 +378,7 @@ __global__ void __launch_bounds__(576, 1)
     uint32_t uit = 0, gblk = 0, item = 0;
     bool ok = true;
     for (uint32_t k = 0; ok; ++k, ++uit) {
-      const int u = take_unit(k, ok, false);
+      const int u = take_unit(k, ok);
       if (u < 0) break;
       int bhk, j;
       unit(u, bhk, j);
@@ -575,14 +581,14 @@ __global__ void __launch_bounds__(576, 1)
     mbar_arrive(bar(ctl.unit_full[slot]));
     return u;
   };
-  auto take_unit = [&](uint32_t k, bool& ok, bool single) -> int {
+  auto take_unit = [&](uint32_t k, bool& ok) -> int {   // a whole warp; lane 0 frees the slot
     const uint32_t slot = k & 3;
     ok = wait_bounded(bar(ctl.unit_full[slot]), (k >> 2) & 1, wc);
-    if (!single) ok = __all_sync(0xffffffffu, ok);
+    ok = __all_sync(0xffffffffu, ok);
     if (!ok) return -1;
     const int u = *reinterpret_cast<volatile int*>(&ctl.unit_ring[slot]);
-    if (!single) __syncwarp();
-    if (single || lane == 0) mbar_arrive(bar(ctl.unit_empty[slot]));
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(ctl.unit_empty[slot]));
     return u;
   };
 
@@ -635,11 +641,16 @@ __global__ void __launch_bounds__(576, 1)
     }
   } else if (warp == C::kEW + 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs this loop converged; one elected lane issues each
+    // MMA and commit (the *_w forms), every wait is taken by all lanes.
+    {
       uint32_t item = 0, uit = 0, gblk = 0;
+      auto wait_w = [&](uint32_t b, uint32_t parity) {
+        return __all_sync(0xffffffffu, wait_bounded(b, parity, wc));
+      };
       bool ok = true;
       auto wait_slot = [&](uint32_t it) {
-        return wait_bounded(bar(ctl.full[it % C::kStagesDQ]), (it / C::kStagesDQ) & 1, wc);
+        return wait_w(bar(ctl.full[it % C::kStagesDQ]), (it / C::kStagesDQ) & 1);
       };
       auto slot_addr = [&](uint32_t it) { return sRing + (it % C::kStagesDQ) * C::kTile; };
       // [128 rows in TMEM at a_col] x [128 rows of the K-major tile b0]^T over K = D
@@ -647,61 +658,62 @@ __global__ void __launch_bounds__(576, 1)
 #pragma unroll
         for (int k = 0; k < C::kSSteps; ++k) {
           const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-          mma_f16_ts(tmem + d_col, tmem + a_col + 8 * k, make_smem_desc(b0 + off, 16, 1024, kSwizzle128B),
-                     C::kIdescSS, k > 0 ? 1u : 0u);
+          mma_f16_ts_w(tmem + d_col, tmem + a_col + 8 * k, make_smem_desc(b0 + off, 16, 1024, kSwizzle128B),
+                       C::kIdescSS, k > 0 ? 1u : 0u);
         }
       };
       for (uint32_t k = 0; ok; ++k, ++uit) {
-        const int u = take_unit(k, ok, true);
+        const int u = take_unit(k, ok);
         if (u < 0) break;
         int bh, i;
         unit(u, bh, i);
         int j_lo, j_hi;
         bwd_krange(i, p, j_lo, j_hi);
         const int J = j_hi - j_lo + 1;
-        if (!(ok = wait_bounded(bar(ctl.fix_full), uit & 1, wc))) break;   // Q_i, dO_i in TMEM
+        if (!(ok = wait_w(bar(ctl.fix_full), uit & 1))) break;   // Q_i, dO_i in TMEM
         const uint32_t base = item;            // K_j item = base + 2jj, V_j = base + 2jj + 1
         item += 2 * J;
         if (!(ok = wait_slot(base) && wait_slot(base + 1))) break;
         tc_fence_after();
         ts_k(kColS, kColQ, slot_addr(base));
-        mma_commit(bar(ctl.s_full));
+        mma_commit_w(bar(ctl.s_full));
         ts_k(kColDP, kColdO, slot_addr(base + 1));
-        mma_commit(bar(ctl.dp_full));
-        mma_commit(bar(ctl.empty[(base + 1) % C::kStagesDQ]));   // V_0 done
+        mma_commit_w(bar(ctl.dp_full));
+        mma_commit_w(bar(ctl.empty[(base + 1) % C::kStagesDQ]));   // V_0 done
         for (int jj = 0; jj < J && ok; ++jj, ++gblk) {
           const uint32_t ik = base + 2 * jj;
           const bool more = jj + 1 < J;
           // S(jj+1) once the element-wise pass has read S(jj)
           if (more) {
-            if (!(ok = wait_bounded(bar(ctl.s_read), gblk & 1, wc) && wait_slot(ik + 2))) break;
+            if (!(ok = wait_w(bar(ctl.s_read), gblk & 1) && wait_slot(ik + 2))) break;
             tc_fence_after();
             ts_k(kColS, kColQ, slot_addr(ik + 2));
-            mma_commit(bar(ctl.s_full));
+            mma_commit_w(bar(ctl.s_full));
           }
           // dQ += dS K_j once dS is written (over dP)
-          if (!(ok = wait_bounded(bar(ctl.p_ready), gblk & 1, wc))) break;
+          if (!(ok = wait_w(bar(ctl.p_ready), gblk & 1))) break;
           tc_fence_after();
           const uint32_t kb = slot_addr(ik);
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             const uint32_t a = tmem + kColDP + (k >> 1) * 32 + (k & 1) * 8;
-            mma_f16_ts(tmem + kColDQ, a, make_smem_desc(kb + k * 2048, 16384, 1024, kSwizzle128B),
-                       C::kIdescTS, (jj > 0 || k > 0) ? 1u : 0u);
+            mma_f16_ts_w(tmem + kColDQ, a, make_smem_desc(kb + k * 2048, 16384, 1024, kSwizzle128B),
+                         C::kIdescTS, (jj > 0 || k > 0) ? 1u : 0u);
           }
-          mma_commit(bar(ctl.empty[ik % C::kStagesDQ]));   // K_j done
+          mma_commit_w(bar(ctl.empty[ik % C::kStagesDQ]));   // K_j done
           // dP(jj+1) over dS(jj): after dQ(jj) in issue order
           if (more) {
             if (!(ok = wait_slot(ik + 3))) break;
             tc_fence_after();
             ts_k(kColDP, kColdO, slot_addr(ik + 3));
-            mma_commit(bar(ctl.dp_full));
-            mma_commit(bar(ctl.empty[(ik + 3) % C::kStagesDQ]));   // V_{jj+1} done
+            mma_commit_w(bar(ctl.dp_full));
+            mma_commit_w(bar(ctl.empty[(ik + 3) % C::kStagesDQ]));   // V_{jj+1} done
           }
         }
-        mma_commit(bar(ctl.unit_done));
+        mma_commit_w(bar(ctl.unit_done));
       }
-      mma_commit(bar(ctl.drain));
+      __syncwarp();
+      mma_commit_w(bar(ctl.drain));
       wait_bounded(bar(ctl.drain), 0, wc, false);
     }
   } else {
@@ -714,7 +726,7 @@ __global__ void __launch_bounds__(576, 1)
     uint32_t uit = 0, gblk = 0;
     bool ok = true;
     for (uint32_t k = 0; ok; ++k, ++uit) {
-      const int u = take_unit(k, ok, false);
+      const int u = take_unit(k, ok);
       if (u < 0) break;
       int bh, i;
       unit(u, bh, i);
