@@ -104,6 +104,7 @@ struct KCfg {
   static constexpr uint32_t kTmemCols = 512;
   static constexpr int kThreads = 320;
   static constexpr float kTau = FP8 ? 0.0f : 8.0f;
+  static constexpr float kSumLimit = 256.0f;              // 2^kTau: bound on a block's sum of p (bf16)
   static constexpr int kSKSteps = FP8 ? D / 32 : D / 16;  // k-steps of S = Q K^T
   static constexpr int kPVSteps = FP8 ? 4 : 8;            // k-steps of O += P V (128 keys)
   static constexpr uint32_t kIdescS =
@@ -118,7 +119,7 @@ struct SmemCtl {
   uint64_t q_full[2];
   uint64_t q_empty[2];
   uint64_t s_full[2];
-  uint64_t p_ready[2][2];   // [tile][half of the block's keys]
+  uint64_t p_ready[2][2];   // [tile][half of the block's keys] (bf16 signals all keys on [t][0])
   uint64_t o_final[2];
   uint64_t drain;
   uint64_t unit_full[4];    // ring of work-unit indices handed out by the load warp
@@ -418,7 +419,8 @@ __global__ void __launch_bounds__(320, 1)
           if (!(ok = wait_w(ctl.p_ready[0][0], pr[0] & 1))) break;
           tc_fence_after();
           pv_mma(0, vslot, j > 0, 0);
-          if (!(ok = wait_w(ctl.p_ready[0][1], pr[0]++ & 1))) break;
+          if (FP8 && !(ok = wait_w(ctl.p_ready[0][1], pr[0] & 1))) break;
+          ++pr[0];
           tc_fence_after();
           pv_mma(0, vslot, j > 0, 1);
           if (j == J - 1) mma_commit_w(bar(ctl.o_final[0]));
@@ -431,7 +433,8 @@ __global__ void __launch_bounds__(320, 1)
           if (!(ok = wait_w(ctl.p_ready[1][0], pr[1] & 1))) break;
           tc_fence_after();
           pv_mma(1, vslot, j > 0, 0);
-          if (!(ok = wait_w(ctl.p_ready[1][1], pr[1]++ & 1))) break;
+          if (FP8 && !(ok = wait_w(ctl.p_ready[1][1], pr[1] & 1))) break;
+          ++pr[1];
           tc_fence_after();
           pv_mma(1, vslot, j > 0, 1);
           mma_commit_w(bar(ctl.kv_empty[vslot]));
@@ -526,9 +529,10 @@ __global__ void __launch_bounds__(320, 1)
           }
         };
         auto row_max = [&](const float (&x)[128]) {
-          float m0 = x[0], m1 = x[1], m2 = x[2], m3 = x[3];
+          float m0 = fmaxf(x[0], x[1]), m1 = fmaxf(x[2], x[3]);
+          float m2 = fmaxf(x[4], x[5]), m3 = fmaxf(x[6], x[7]);
 #pragma unroll
-          for (int c = 4; c < 128; c += 8) {
+          for (int c = 8; c < 128; c += 8) {
             m0 = max3(m0, x[c], x[c + 1]);
             m1 = max3(m1, x[c + 2], x[c + 3]);
             m2 = max3(m2, x[c + 4], x[c + 5]);
@@ -594,35 +598,27 @@ __global__ void __launch_bounds__(320, 1)
           f32x2_unpack(f32x2_add(s01, s23), a0, a1);
           ell += (a0 + a1) / v_fold;
         } else {
-          // p = 2^(s*c - m) against the running reference max m, with the block's
-          // own max taken in the same pass, so no exponential waits for a max.
-          // The pass stands unless the block's max rose more than tau above m
-          // (rare after the first block); then m moves to the block's max, O and
-          // the sums are rescaled and the block (still in TMEM: P has not been
-          // stored yet) is taken again.  P is rounded to bf16 for the PV MMA; the
-          // sum of exactly those rounded values (l~) normalises O, so numerator
-          // and denominator use the same weights, while the sum of the f32 values
-          // (l) gives the logsumexp.
+          // p = 2^(s*c - m) against the running reference max m, so no
+          // exponential waits for the block's max.  The block's sum of p bounds
+          // every p in it: if the sum is at most 2^tau the pass stands (p <=
+          // 2^tau, as the reference rule requires).  Otherwise (rare after the
+          // first block: the block's max is then more than 1 above m) m moves to
+          // the block's max, O and the sums are rescaled and the block (still in
+          // TMEM: P has not been stored yet) is taken again.  P is rounded to
+          // bf16 for the PV MMA; the sum of exactly those rounded values (l~)
+          // normalises O, so numerator and denominator use the same weights,
+          // while the sum of the f32 values (l) gives the logsumexp.
           uint32_t pk[64];
           float e_sum, r_sum;
           // A row that has seen no visible key yet (every row at a unit's first
           // block) takes its reference from this block's max before the pass;
           // its O and sums are still 0, so nothing is rescaled.
-          bool pre = !__all_sync(0xffffffffu, m_ref != NEG_INF);
-          for (;;) {
-            float x[128];
-            load_s(x);
-            if (pre) {
-              const float m_blk0 = row_max(x) * cj;
-              if (m_ref == NEG_INF) m_ref = m_blk0;
-              pre = false;
-            }
+          auto exps = [&](const float (&x)[128]) {
             const float m_use = (m_ref == NEG_INF) ? 0.0f : m_ref;
             const uint64_t c2 = f32x2_pack(cj, cj);
             const uint64_t nm2 = f32x2_pack(-m_use, -m_use);
             uint64_t ex0 = 0, ex1 = 0;   // (0.f, 0.f)
             float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
-            float m0 = NEG_INF, m1 = NEG_INF, m2 = NEG_INF, m3 = NEG_INF;
 #pragma unroll
             for (int i = 0; i < 64; ++i) {
               float t0, t1;
@@ -631,12 +627,6 @@ __global__ void __launch_bounds__(320, 1)
               const uint32_t pb = pack_bf16x2(p0, p1);
               pk[i] = pb;
               const uint64_t e = f32x2_pack(p0, p1);
-              switch (i & 3) {
-                case 0: m0 = max3(m0, x[2 * i], x[2 * i + 1]); break;
-                case 1: m1 = max3(m1, x[2 * i], x[2 * i + 1]); break;
-                case 2: m2 = max3(m2, x[2 * i], x[2 * i + 1]); break;
-                default: m3 = max3(m3, x[2 * i], x[2 * i + 1]); break;
-              }
               if (i & 1) {
                 r2 = add_bf16_lo(pb, r2);
                 r3 = add_bf16_hi(pb, r3);
@@ -647,30 +637,45 @@ __global__ void __launch_bounds__(320, 1)
                 ex0 = f32x2_add(ex0, e);
               }
             }
-            const float m_blk = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)) * cj;
-            const bool need = m_blk > m_ref + tau;
-            if (!__any_sync(0xffffffffu, need)) {
-              float b0, b1;
-              f32x2_unpack(f32x2_add(ex0, ex1), b0, b1);
-              e_sum = b0 + b1;
-              r_sum = (r0 + r1) + (r2 + r3);
-              break;
+            float b0, b1;
+            f32x2_unpack(f32x2_add(ex0, ex1), b0, b1);
+            e_sum = b0 + b1;
+            r_sum = (r0 + r1) + (r2 + r3);
+          };
+          {
+            float x[128];
+            load_s(x);
+            // A row that has seen no visible key yet (every row at a unit's
+            // first block) takes its reference from this block's max first; its
+            // O and sums are still 0, so nothing is rescaled.
+            if (!__all_sync(0xffffffffu, m_ref != NEG_INF)) {
+              const float m_blk0 = row_max(x) * cj;
+              if (m_ref == NEG_INF) m_ref = m_blk0;
             }
-            const float alpha = need ? ex2_approx(m_ref - m_blk) : 1.0f;
+            exps(x);
+          }
+          // A sum of 128 terms above 2^tau = 256 has a term above 2; moving m to
+          // the block's max makes every term <= 1, so one more pass suffices.
+          const bool redo = !(e_sum <= C::kSumLimit);
+          if (__any_sync(0xffffffffu, redo)) {
+            float x[128];
+            load_s(x);
+            const float m_blk = row_max(x) * cj;
+            const float m_new = redo ? fmaxf(m_ref, m_blk) : m_ref;
+            const float alpha = ex2_approx(m_ref - m_new);
             if (jj > 0) rescale_o(alpha);
             ell *= alpha;
             ell_r *= alpha;
-            if (need) m_ref = m_blk;
+            m_ref = m_new;
+            exps(x);
           }
           __syncwarp();   // tcgen05.st is warp-collective
           tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
           tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
-          // bf16: one signal for both halves of the keys (a half's PV is as long
-          // as the exponentials it could overlap; the extra wait costs more).
+          // bf16: one signal for all keys of the block (P·V waits for it once).
           tmem_wait_st();
           tc_fence_before();
           mbar_arrive(bar(ctl.p_ready[t][0]));
-          mbar_arrive(bar(ctl.p_ready[t][1]));
           ell_r += r_sum;
           ell += e_sum;
         }
