@@ -45,8 +45,9 @@
 // FP8 variant (E4M3 operands, f32 accumulation): per-128-row block scales of
 // Q, K, V ("FlashAttention-3: How Warp Specialization ...", section 4); the
 // score scale of block j is folded into the exp2 factor, P is quantised to
-// E4M3 as p * 256 * s_V(j) / max_j s_V(j) (tau = 0 so p <= 1), which folds
-// V's per-block scale into P, and the epilogue divides by 256 * l / max s_V.
+// E4M3 as p * 64 * s_V(j) / max_j s_V(j) (tau = 2 so p <= 4 and P <= 256,
+// inside E4M3's 448), which folds V's per-block scale into P, and the
+// epilogue divides by 64 * l / max s_V.
 // V arrives transposed ([d][N], keys contiguous) so both MMAs read K-major
 // operands.
 #pragma once
@@ -103,7 +104,8 @@ struct KCfg {
   static constexpr int kSmemBytes = (2 + kStages) * kTileBytes + 1024;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr int kThreads = 320;
-  static constexpr float kTau = FP8 ? 0.0f : 8.0f;
+  static constexpr float kTau = FP8 ? 2.0f : 8.0f;
+  static constexpr float kPScale = 64.0f;                 // FP8: P' = p * kPScale * s_V(j) / max s_V <= 2^kTau * 64 = 256
   static constexpr float kSumLimit = 256.0f;              // 2^kTau: bound on a block's sum of p (bf16)
   static constexpr int kSKSteps = FP8 ? D / 32 : D / 16;  // k-steps of S = Q K^T
   static constexpr int kPVSteps = FP8 ? 4 : 8;            // k-steps of O += P V (128 keys)
@@ -508,7 +510,7 @@ __global__ void __launch_bounds__(320, 1)
         float v_fold = 1.0f;
         if (FP8) {
           cj *= q_s * __ldg(p.k_scale + (size_t)w.bhk * p.nkb + j);
-          v_fold = 256.0f * __ldg(p.v_scale + (size_t)w.bhk * p.nkb + j) / v_smax;
+          v_fold = C::kPScale * __ldg(p.v_scale + (size_t)w.bhk * p.nkb + j) / v_smax;
         }
         const int lim = lim_row - j * 128;    // columns > lim are invisible
         const int lo = lo_row - j * 128;      // columns < lo are invisible (window)
@@ -555,7 +557,7 @@ __global__ void __launch_bounds__(320, 1)
         };
         if constexpr (FP8) {
           // FP8 P must stay within E4M3's range, so the block max is taken first
-          // and the reference follows it exactly (tau = 0).
+          // and the reference moves whenever it rises by more than tau = 2.
           float x[128];
           load_s(x);
           const float m_blk = row_max(x) * cj;
@@ -688,7 +690,7 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_after();
       float inv;
       if (FP8)
-        inv = (ell > 0.0f) ? v_smax * (1.0f / 256.0f) / ell : 0.0f;
+        inv = (ell > 0.0f) ? v_smax / C::kPScale / ell : 0.0f;
       else
         inv = (ell_r > 0.0f) ? 1.0f / ell_r : 0.0f;
       const bool live = row < p.N;
