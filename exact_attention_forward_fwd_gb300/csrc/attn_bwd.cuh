@@ -400,8 +400,7 @@ __global__ void __launch_bounds__(576, 1)
         // block's dS^T is signalled, so the phase test is unambiguous.
         if (ok) ok = wait_bounded(bar(ctl.full[item % C::kStages]), (item / C::kStages) & 1, wc);
         ok = __all_sync(0xffffffffu, ok);
-        ok = bar_and(1, 32 * C::kEW, ok);
-        if (!ok) break;
+        if (!ok) break;   // a timed-out wait also set the abort flag every other wait honours
         tc_fence_after();
         // ---- phase A: P^T = exp2(S^T * c - L') for this thread's 32 queries
         float pr[32];
@@ -772,8 +771,7 @@ __global__ void __launch_bounds__(576, 1)
         // Exponentials as soon as S is there; dS once dP is there too.
         ok = wait_bounded(bar(ctl.s_full), gblk & 1, wc);
         ok = __all_sync(0xffffffffu, ok);
-        ok = bar_and(1, 32 * C::kEW, ok);
-        if (!ok) break;
+        if (!ok) break;   // a timed-out wait also set the abort flag every other wait honours
         tc_fence_after();
         float pr[32];
         {

@@ -74,21 +74,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Named barrier over `count` threads with an AND-reduction of a predicate:
-// every participant gets true only if all of them passed true.
-__device__ __forceinline__ bool bar_and(uint32_t id, uint32_t count, bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %3, 0;\n\t"
-      "bar.red.and.pred q, %1, %2, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}\n"
-      : "=r"(r)
-      : "r"(id), "r"(count), "r"(pred ? 1u : 0u)
-      : "memory");
-  return r != 0;
-}
-
 // ---------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
