@@ -243,7 +243,11 @@ def attn_fwd_splitkv_static(q, k, v, causal: bool = False, window: int = 0,
                             scale: float | None = None, num_splits: int | None = None, out=None,
                             lse=None, return_lse: bool = True):
     """attn_fwd_splitkv on the library's own 64 MiB scratch array: the C call
-    allocates nothing.  Calls must not overlap in time.  Returns (O, lse)."""
+    allocates nothing, for callers that cannot call cudaMalloc (a host program
+    that owns all device memory through its own pool, or a loop that must not
+    take cudaMalloc's device-wide synchronisation).  Pass ``out`` and ``lse`` to
+    keep this wrapper from allocating them through torch.  Calls share the one
+    array and must not overlap in time.  Returns (O, lse)."""
     torch = _torch()
     for name, t in (("q", q), ("k", k), ("v", v)):
         _need(t, name, torch.bfloat16)

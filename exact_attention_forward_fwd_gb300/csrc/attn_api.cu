@@ -98,7 +98,10 @@ struct SplitArgs {
 };
 
 // Scratch of attn_fwd_splitkv_static: a file-scope device array (no allocation
-// call anywhere), its address looked up once per device.
+// call anywhere).  In host code g_splitkv_scratch names a host-side shadow, not
+// device memory, so the device address is looked up with cudaGetSymbolAddress
+// once per device (with that device current) and that address is what the
+// kernels get.  Every call shares the array; calls that overlap on the GPU race.
 constexpr size_t kStaticScratchBytes = size_t(64) << 20;
 static __device__ __align__(256) unsigned char g_splitkv_scratch[kStaticScratchBytes];
 std::mutex g_scratch_mu;

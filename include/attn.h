@@ -120,8 +120,12 @@ ATTN_API int attn_fwd_splitkv(const void* q, const void* k, const void* v, void*
  * partial results go to one scratch array of 64 MiB (67108864 bytes) that the
  * library defines as a file-scope device variable, so it exists on every
  * device the library's code is loaded on.  The pages have no counterpart to
- * this entry point; it serves callers that must not allocate, e.g. inside a
- * captured CUDA graph.
+ * this entry point.  It is for callers that cannot call cudaMalloc: a plugin
+ * running inside a host program that owns every byte of device memory through
+ * its own pool (and may fail or fragment it if a library allocates behind its
+ * back), or a latency-bound serving loop that must not pay cudaMalloc's implicit
+ * device-wide synchronisation.  The price is 64 MiB held on every device that
+ * loads the library, until the process exits.
  *   Arguments and errors: as attn_fwd_splitkv, minus the workspace;
  *   ATTN_ERR_INVALID_ARG also when attn_splitkv_workspace_bytes(B, H, N, d,
  *   num_splits) exceeds 64 MiB (nothing is launched).
@@ -130,8 +134,9 @@ ATTN_API int attn_fwd_splitkv(const void* q, const void* k, const void* v, void*
  *   Calls share the one array: two calls that overlap in time (different
  *   streams or host threads without ordering) race and give undefined
  *   results; order them.  The first call on each device looks the array's
- *   address up (cudaGetSymbolAddress, ATTN_ERR_CUDA if that fails); make that
- *   first call before capturing the stream into a graph. */
+ *   address up (cudaGetSymbolAddress with that device current, ATTN_ERR_CUDA
+ *   if that fails); that first call should come before any stream capture.
+ *   The call makes no cudaMalloc, cudaFree or other allocating call. */
 ATTN_API int attn_fwd_splitkv_static(const void* q, const void* k, const void* v, void* o,
                                      float* lse, int B, int H, int H_kv, int N, int d,
                                      float scale, int causal, int window, int dtype,
