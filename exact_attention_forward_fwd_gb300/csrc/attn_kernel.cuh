@@ -31,13 +31,15 @@
 //   * scale folded into exp2: p = 2^(s * scale*log2(e) - m), m kept in the
 //     same base-2 units;
 //   * conditional rescaling: the reference max used for the exponentials is
-//     only moved (and O~, l rescaled) when the block max exceeds it by more
-//     than tau (base-2 units).  Numerator and denominator always share the
-//     same reference, so the result stays exact; p <= 2^tau.  The bf16 path
-//     takes the exponentials against the current reference and the block max
-//     in one pass, and takes the block again in the rare case the max moved
-//     by more than tau (S is still in TMEM then), so no exponential waits
-//     for a row max.
+//     only moved (and O~, l rescaled) when the block's values against it grow
+//     too large.  Numerator and denominator always share the same reference,
+//     so the result stays exact.  The exponentials are taken against the
+//     current reference and the block's sum of p decides: a sum of at most
+//     2^8 bounds every p by 2^8 and the pass stands; otherwise (rare after a
+//     unit's first block) the reference moves to the block's max and the
+//     block, still in TMEM, is taken again.  No exponential waits for a row
+//     max.  The FP8 path takes the block's max first instead and moves the
+//     reference only when that max exceeds it by more than 8, so p <= 2^8.
 //   * because every tcgen05.commit tracks all earlier MMAs of the issuing
 //     thread, the arrival of S_t(j) also proves O_t += P_t(j-1) V(j-1) is
 //     complete: a rescale of O~ right after waiting for S_t(j) is race-free.
@@ -45,9 +47,9 @@
 // FP8 variant (E4M3 operands, f32 accumulation): per-128-row block scales of
 // Q, K, V ("FlashAttention-3: How Warp Specialization ...", section 4); the
 // score scale of block j is folded into the exp2 factor, P is quantised to
-// E4M3 as p * 64 * s_V(j) / max_j s_V(j) (tau = 2 so p <= 4 and P <= 256,
-// inside E4M3's 448), which folds V's per-block scale into P, and the
-// epilogue divides by 64 * l / max s_V.
+// E4M3 as p * 1.75 * s_V(j) / max_j s_V(j) (p <= 2^8, so P <= 448, E4M3's
+// largest finite value), which folds V's per-block scale into P, and the
+// epilogue divides by 1.75 * l / max s_V.
 // V arrives transposed ([d][N], keys contiguous) so both MMAs read K-major
 // operands.
 #pragma once
@@ -104,9 +106,9 @@ struct KCfg {
   static constexpr int kSmemBytes = (2 + kStages) * kTileBytes + 1024;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr int kThreads = 320;
-  static constexpr float kTau = FP8 ? 2.0f : 8.0f;
-  static constexpr float kPScale = 64.0f;                 // FP8: P' = p * kPScale * s_V(j) / max s_V <= 2^kTau * 64 = 256
-  static constexpr float kSumLimit = 256.0f;              // 2^kTau: bound on a block's sum of p (bf16)
+  static constexpr float kSumLimit = 256.0f;              // 2^8: bound on a block's sum of p
+  static constexpr float kTauLog2 = 8.0f;                 // FP8: move the reference when a block max exceeds it by more
+  static constexpr float kPScale = 1.75f;                 // FP8: P' = p * kPScale * s_V(j) / max s_V <= 256 * 1.75 = 448
   static constexpr int kSKSteps = FP8 ? D / 32 : D / 16;  // k-steps of S = Q K^T
   static constexpr int kPVSteps = FP8 ? 4 : 8;            // k-steps of O += P V (128 keys)
   static constexpr uint32_t kIdescS =
@@ -359,35 +361,39 @@ __global__ void __launch_bounds__(320, 1)
       auto wait_w = [&](uint64_t& b, uint32_t parity) {
         return __all_sync(0xffffffffu, wait_bounded(bar(b), parity, wc));
       };
+      // Descriptor bases, computed once: K-major Q and K tiles (and FP8 V^T),
+      // MN-major bf16 V tiles.  A k-step adds its offset in 16-byte units to
+      // the address field (tiles lie below 256 KB, so it never carries).
+      constexpr uint64_t kTileUnits = C::kTileBytes >> 4;
+      const uint64_t dQ = make_smem_desc(sQ, 16, 1024, kSwizzle128B);
+      const uint64_t dK = make_smem_desc(sKV, 16, 1024, kSwizzle128B);
+      const uint64_t dV = make_smem_desc(sKV, FP8 ? 16 : 16384, 1024, kSwizzle128B);
       auto s_mma = [&](int t, uint32_t kslot) {
-        const uint32_t a0 = sQ + t * C::kTileBytes;
-        const uint32_t b0 = sKV + kslot * C::kTileBytes;
+        const uint64_t da = dQ + t * kTileUnits;
+        const uint64_t db = dK + kslot * kTileUnits;
 #pragma unroll
-        for (int k = 0; k < C::kSKSteps; ++k) {
-          const uint32_t off = FP8 ? k * 32 : (k >> 2) * 16384 + (k & 3) * 32;
-          const uint64_t da = make_smem_desc(a0 + off, 16, 1024, kSwizzle128B);
-          const uint64_t db = make_smem_desc(b0 + off, 16, 1024, kSwizzle128B);
-          if (FP8)
-            mma_f8_ss_w(tmem + 128 * t, da, db, C::kIdescS, k > 0);
-          else
-            mma_f16_ss_w(tmem + 128 * t, da, db, C::kIdescS, k > 0);
+        for (int g = 0; g < C::kSKSteps / 4; ++g) {
+          const uint64_t o = FP8 ? 0 : g * 1024;   // next 128-byte column slab (bf16, d = 128)
+          mma_ss_x4_w<FP8>(tmem + 128 * t, da + o, da + o + 2, da + o + 4, da + o + 6, db + o,
+                           db + o + 2, db + o + 4, db + o + 6, C::kIdescS, g > 0 ? 1u : 0u);
         }
       };
       // O_t += P_t V over the keys of half `hf` of the block (P of each half is
       // signalled separately, so the first half's product overlaps the
       // exponentials of the second).
       auto pv_mma = [&](int t, uint32_t vslot, bool acc, int hf) {
-        const uint32_t b0 = sKV + vslot * C::kTileBytes;
-#pragma unroll
-        for (int k = hf * (C::kPVSteps / 2); k < (hf + 1) * (C::kPVSteps / 2); ++k) {
-          const uint32_t a = tmem + 128 * t + k * 8;
-          if (FP8) {
-            const uint64_t db = make_smem_desc(b0 + k * 32, 16, 1024, kSwizzle128B);
-            mma_f8_ts_w(tmem + 256 + D * t, a, db, C::kIdescPV, (acc || k > 0) ? 1u : 0u);
-          } else {
-            const uint64_t db = make_smem_desc(b0 + k * 2048, 16384, 1024, kSwizzle128B);
-            mma_f16_ts_w(tmem + 256 + D * t, a, db, C::kIdescPV, (acc || k > 0) ? 1u : 0u);
-          }
+        const uint64_t db = dV + vslot * kTileUnits;
+        const uint32_t ta = tmem + 128 * t;
+        const uint32_t acc0 = (acc || hf > 0) ? 1u : 0u;
+        if constexpr (FP8) {
+          const int k = 2 * hf;
+          mma_f8_ts_w(tmem + 256 + D * t, ta + k * 8, db + k * 2, C::kIdescPV, acc0);
+          mma_f8_ts_w(tmem + 256 + D * t, ta + k * 8 + 8, db + k * 2 + 2, C::kIdescPV, 1u);
+        } else {
+          const int k = 4 * hf;   // 16-key steps: P columns advance by 8, V rows by 2048 bytes
+          mma_ts_x4_w<false>(tmem + 256 + D * t, ta + k * 8, ta + k * 8 + 8, ta + k * 8 + 16,
+                             ta + k * 8 + 24, db + k * 128, db + k * 128 + 128, db + k * 128 + 256,
+                             db + k * 128 + 384, C::kIdescPV, acc0);
         }
       };
       auto wait_item = [&](uint32_t it) {
@@ -466,7 +472,6 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + lane_off + 128 * t;
     const uint32_t tO = tmem + lane_off + 256 + D * t;
-    const float tau = C::kTau;
     const float NEG_INF = __int_as_float(0xff800000);
     uint32_t sit = 0, uit = 0;
     bool ok = true;
@@ -556,31 +561,22 @@ __global__ void __launch_bounds__(320, 1)
           }
         };
         if constexpr (FP8) {
-          // FP8 P must stay within E4M3's range, so the block max is taken first
-          // and the reference moves whenever it rises by more than tau = 2.
-          float x[128];
-          load_s(x);
-          const float m_blk = row_max(x) * cj;
-          const bool need = m_blk > m_ref + tau;
-          const float m_new = need ? m_blk : m_ref;
-          const float alpha = need ? ex2_approx(m_ref - m_new) : 1.0f;   // 0 when m_ref = -inf
-          if (jj > 0 && __any_sync(0xffffffffu, need)) rescale_o(alpha);
-          ell *= alpha;
-          m_ref = m_new;
-          const float m_use = (m_ref == NEG_INF) ? 0.0f : m_ref;
-          __syncwarp();   // tcgen05.st is warp-collective: reconverge after the mask branch
-          // p' = p * v_fold = 2^(s c - (m - log2 v_fold)): V's block scale rides in
-          // the exponent, and the block's sum of p is sum(p') / v_fold.
-          const float m_f = m_use - __log2f(v_fold);
-          const uint64_t c2 = f32x2_pack(cj, cj);
-          const uint64_t nm2 = f32x2_pack(-m_f, -m_f);
-          uint64_t s01 = 0, s23 = 0;   // (0.f, 0.f)
+          // p' = p * v_fold = 2^(s c - (m - log2 v_fold)) against the running
+          // reference m (V's block scale rides in the exponent).  m moves to the
+          // block's max only when that max exceeds m by more than 8 (base 2), so
+          // p <= 2^8 and P' = p * v_fold <= 256 * kPScale = 448, inside E4M3's
+          // range.
+          uint32_t pk[32];
+          float e_sum;
+          auto exps = [&](const float (&x)[128]) {
+            const float m_use = (m_ref == NEG_INF) ? 0.0f : m_ref;
+            const float m_f = m_use - __log2f(v_fold);
+            const uint64_t c2 = f32x2_pack(cj, cj);
+            const uint64_t nm2 = f32x2_pack(-m_f, -m_f);
+            uint64_t s01 = 0, s23 = 0;   // (0.f, 0.f)
 #pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const int c = 64 * hf + 4 * i;
+            for (int i = 0; i < 32; ++i) {
+              const int c = 4 * i;
               float t0, t1, t2, t3;
               f32x2_unpack(f32x2_fma(f32x2_pack(x[c], x[c + 1]), c2, nm2), t0, t1);
               f32x2_unpack(f32x2_fma(f32x2_pack(x[c + 2], x[c + 3]), c2, nm2), t2, t3);
@@ -590,15 +586,36 @@ __global__ void __launch_bounds__(320, 1)
               s23 = f32x2_add(s23, f32x2_pack(p2, p3));
               pk[i] = pack_e4m3x4(p0, p1, p2, p3);
             }
-            // keys [64hf, 64hf+64) -> columns [16hf, 16hf+16)
-            tmem_st16(tS + 16 * hf, pk);
+            float a0, a1;
+            f32x2_unpack(f32x2_add(s01, s23), a0, a1);
+            e_sum = (a0 + a1) / v_fold;
+          };
+          {
+            // The block's max first: E4M3 P must never saturate, and with the
+            // outliers FP8 inputs carry, large rises of a row's max are common
+            // enough that retaking a block would cost more than this pass.
+            float x[128];
+            load_s(x);
+            const float m_blk = row_max(x) * cj;
+            const bool need = m_blk > m_ref + C::kTauLog2;
+            const float m_new = need ? m_blk : m_ref;
+            const float alpha = need ? ex2_approx(m_ref - m_new) : 1.0f;   // 0 when m_ref = -inf
+            if (jj > 0 && __any_sync(0xffffffffu, need)) rescale_o(alpha);
+            ell *= alpha;
+            m_ref = m_new;
+            exps(x);
+          }
+          __syncwarp();   // tcgen05.st is warp-collective
+          // keys [64hf, 64hf+64) -> columns [16hf, 16hf+16), one signal each, so
+          // the first half's P.V can start while the second half is stored
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            tmem_st16(tS + 16 * hf, *reinterpret_cast<uint32_t(*)[16]>(&pk[16 * hf]));
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(bar(ctl.p_ready[t][hf]));
           }
-          float a0, a1;
-          f32x2_unpack(f32x2_add(s01, s23), a0, a1);
-          ell += (a0 + a1) / v_fold;
+          ell += e_sum;
         } else {
           // p = 2^(s*c - m) against the running reference max m, so no
           // exponential waits for the block's max.  The block's sum of p bounds
@@ -664,7 +681,7 @@ __global__ void __launch_bounds__(320, 1)
             load_s(x);
             const float m_blk = row_max(x) * cj;
             const float m_new = redo ? fmaxf(m_ref, m_blk) : m_ref;
-            const float alpha = ex2_approx(m_ref - m_new);
+            const float alpha = redo ? ex2_approx(m_ref - m_new) : 1.0f;
             if (jj > 0) rescale_o(alpha);
             ell *= alpha;
             ell_r *= alpha;

@@ -316,6 +316,65 @@ __device__ __forceinline__ void mma_f8_ts_w(uint32_t d_tmem, uint32_t a_tmem, ui
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate));
 }
 
+// Several MMAs into one accumulator under a single election (warp-wide form):
+// the first accumulates only if `accumulate` is non-zero, the others always.
+// SS: A and B from shared-memory descriptors; TS: A from tensor memory.
+#define GB300_MMA_KIND_F16 "kind::f16"
+#define GB300_MMA_KIND_F8 "kind::f8f6f4"
+template <bool F8>
+__device__ __forceinline__ void mma_ss_x4_w(uint32_t d_tmem, uint64_t a0, uint64_t a1, uint64_t a2,
+                                            uint64_t a3, uint64_t b0, uint64_t b1, uint64_t b2,
+                                            uint64_t b3, uint32_t idesc, uint32_t accumulate) {
+  if constexpr (F8) {
+    asm volatile(
+        "{\n\t.reg .pred p, q, e;\n\tsetp.ne.b32 p, %10, 0;\n\tsetp.eq.b32 q, %9, %9;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1." GB300_MMA_KIND_F8 " [%0], %1, %5, %9, p;\n\t"
+        "@e tcgen05.mma.cta_group::1." GB300_MMA_KIND_F8 " [%0], %2, %6, %9, q;\n\t"
+        "@e tcgen05.mma.cta_group::1." GB300_MMA_KIND_F8 " [%0], %3, %7, %9, q;\n\t"
+        "@e tcgen05.mma.cta_group::1." GB300_MMA_KIND_F8 " [%0], %4, %8, %9, q;\n\t}\n" ::"r"(d_tmem),
+        "l"(a0), "l"(a1), "l"(a2), "l"(a3), "l"(b0), "l"(b1), "l"(b2), "l"(b3), "r"(idesc),
+        "r"(accumulate));
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p, q, e;\n\tsetp.ne.b32 p, %10, 0;\n\tsetp.eq.b32 q, %9, %9;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1." GB300_MMA_KIND_F16 " [%0], %1, %5, %9, p;\n\t"
+        "@e tcgen05.mma.cta_group::1." GB300_MMA_KIND_F16 " [%0], %2, %6, %9, q;\n\t"
+        "@e tcgen05.mma.cta_group::1." GB300_MMA_KIND_F16 " [%0], %3, %7, %9, q;\n\t"
+        "@e tcgen05.mma.cta_group::1." GB300_MMA_KIND_F16 " [%0], %4, %8, %9, q;\n\t}\n" ::"r"(d_tmem),
+        "l"(a0), "l"(a1), "l"(a2), "l"(a3), "l"(b0), "l"(b1), "l"(b2), "l"(b3), "r"(idesc),
+        "r"(accumulate));
+  }
+}
+
+template <bool F8>
+__device__ __forceinline__ void mma_ts_x4_w(uint32_t d_tmem, uint32_t a0, uint32_t a1, uint32_t a2,
+                                            uint32_t a3, uint64_t b0, uint64_t b1, uint64_t b2,
+                                            uint64_t b3, uint32_t idesc, uint32_t accumulate) {
+  if constexpr (F8) {
+    asm volatile(
+        "{\n\t.reg .pred p, q, e;\n\tsetp.ne.b32 p, %10, 0;\n\tsetp.eq.b32 q, %9, %9;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1." GB300_MMA_KIND_F8 " [%0], [%1], %5, %9, p;\n\t"
+        "@e tcgen05.mma.cta_group::1." GB300_MMA_KIND_F8 " [%0], [%2], %6, %9, q;\n\t"
+        "@e tcgen05.mma.cta_group::1." GB300_MMA_KIND_F8 " [%0], [%3], %7, %9, q;\n\t"
+        "@e tcgen05.mma.cta_group::1." GB300_MMA_KIND_F8 " [%0], [%4], %8, %9, q;\n\t}\n" ::"r"(d_tmem),
+        "r"(a0), "r"(a1), "r"(a2), "r"(a3), "l"(b0), "l"(b1), "l"(b2), "l"(b3), "r"(idesc),
+        "r"(accumulate));
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p, q, e;\n\tsetp.ne.b32 p, %10, 0;\n\tsetp.eq.b32 q, %9, %9;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1." GB300_MMA_KIND_F16 " [%0], [%1], %5, %9, p;\n\t"
+        "@e tcgen05.mma.cta_group::1." GB300_MMA_KIND_F16 " [%0], [%2], %6, %9, q;\n\t"
+        "@e tcgen05.mma.cta_group::1." GB300_MMA_KIND_F16 " [%0], [%3], %7, %9, q;\n\t"
+        "@e tcgen05.mma.cta_group::1." GB300_MMA_KIND_F16 " [%0], [%4], %8, %9, q;\n\t}\n" ::"r"(d_tmem),
+        "r"(a0), "r"(a1), "r"(a2), "r"(a3), "l"(b0), "l"(b1), "l"(b2), "l"(b3), "r"(idesc),
+        "r"(accumulate));
+  }
+}
+
 __device__ __forceinline__ void mma_commit_w(uint32_t bar) {
   asm volatile(
       "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"

@@ -180,7 +180,8 @@ ATTN_API int attn_fp8_prep(const void* x, void* x8, float* block_scale, const si
 /* Exact attention forward with E4M3 operands (f32 accumulation, f32 softmax
  * statistics, bf16 output).  Score tile j of query block i is
  * q_scale[i] * k_scale[j] * (Q8_i K8_j^T) * scale.  P is quantised to E4M3
- * with V's block scale folded in (p * 256 * v_scale[j] / max_j v_scale[j]).
+ * with V's block scale folded in (p * 1.75 * v_scale[j] / max_j v_scale[j],
+ * p <= 2^8 against the running reference maximum, so P' <= 448).
  *   q8, k8  : E4M3 [B, H, N, d] from attn_fp8_prep (same signs for both).
  *   v8t     : E4M3 [B, H, d, Npad] from attn_fp8_prep with transpose_out = 1.
  *   q_scale, k_scale, v_scale : f32 [B, H, ceil(N/128)] block scales.
