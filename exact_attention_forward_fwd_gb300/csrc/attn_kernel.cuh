@@ -105,7 +105,15 @@ struct KCfg {
   static constexpr int kStages = (kTileBytes == 32768) ? 4 : 8;
   static constexpr int kSmemBytes = (2 + kStages) * kTileBytes + 1024;
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr int kThreads = 320;
+  // 12 warps: two softmax warpgroups (warps 0-7), then load (8), MMA (9) and
+  // two idle warps (10, 11) that complete the third warpgroup so that it can
+  // hand its registers to the softmax warpgroups.
+  static constexpr int kThreads = 384;
+  static constexpr int kLaunchRegs = 168;                 // 65536 / 384, rounded down to 8
+  static constexpr uint32_t kRegsSoftmax = 224;
+  static constexpr uint32_t kRegsOther = 56;
+  static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsOther <= kThreads * kLaunchRegs,
+                "register split exceeds the block's pool");
   static constexpr float kSumLimit = 256.0f;              // 2^8: bound on a block's sum of p
   static constexpr float kTauLog2 = 8.0f;                 // FP8: move the reference when a block max exceeds it by more
   static constexpr float kPScale = 1.75f;                 // FP8: P' = p * kPScale * s_V(j) / max s_V <= 256 * 1.75 = 448
@@ -217,7 +225,7 @@ __device__ __forceinline__ Unit unit_of(int u, const AttnParams& p) {
 }
 
 template <int D, bool FP8>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(384, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
   using C = KCfg<D, FP8>;
@@ -287,8 +295,11 @@ __global__ void __launch_bounds__(320, 1)
     return u;
   };
 
+  // Each role sets its warpgroup's register budget first (warps 8-11 give
+  // registers up, warps 0-7 take them).
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
+    regs_dec<C::kRegsOther>();
     if (lane == 0) {
       prefetch_tensormap(&tmQ);
       prefetch_tensormap(&tmK);
@@ -353,6 +364,7 @@ __global__ void __launch_bounds__(320, 1)
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
+    regs_dec<C::kRegsOther>();
     // The whole warp runs this loop converged; each MMA and commit is issued by
     // one elected lane (the *_w forms), every wait is taken by all lanes.
     {
@@ -464,8 +476,9 @@ __global__ void __launch_bounds__(320, 1)
       mma_commit_w(bar(ctl.drain));
       wait_bounded(bar(ctl.drain), 0, wc, false);
     }
-  } else {
+  } else if (warp < 8) {
     // ------------------------------------------------------------ softmax
+    regs_inc<C::kRegsSoftmax>();
     const int t = warp >> 2;                 // query tile of the pair
     const int wq = warp & 3;                 // TMEM lane quarter
     const int r = wq * 32 + lane;            // row within the tile
@@ -756,6 +769,8 @@ __global__ void __launch_bounds__(320, 1)
       ++uit;
       // The next unit's first P arrive (after this epilogue) releases O_t.
     }
+  } else {
+    regs_dec<C::kRegsOther>();   // warps 10, 11: no role
   }
 
   tc_fence_before();
@@ -807,6 +822,12 @@ cudaError_t launch_attn(const CUtensorMap& q, const CUtensorMap& k, const CUtens
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
+  // The register split inside the kernel draws on the pool the launch
+  // allocates; refuse to launch a build whose register count would leave the
+  // softmax warps' increase waiting forever.
+  cudaFuncAttributes fa{};
+  if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
+  if (fa.numRegs < C::kLaunchRegs) return cudaErrorInvalidConfiguration;
   AttnParams pd = p;
   if ((e = unit_counter(stream, &pd.sched)) != cudaSuccess) return e;
   cudaLaunchConfig_t cfg{};

@@ -316,6 +316,18 @@ __device__ __forceinline__ void mma_f8_ts_w(uint32_t d_tmem, uint32_t a_tmem, ui
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate));
 }
 
+// Per-warpgroup register budget (every warp of a warpgroup executes the same
+// one).  An increase waits until the block's pool, fixed at launch (threads x
+// registers per thread), has the registers; decreases return them to it.
+template <uint32_t R>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R));
+}
+template <uint32_t R>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R));
+}
+
 // Several MMAs into one accumulator under a single election (warp-wide form):
 // the first accumulates only if `accumulate` is non-zero, the others always.
 // SS: A and B from shared-memory descriptors; TS: A from tensor memory.
