@@ -294,23 +294,30 @@ __global__ void __launch_bounds__(576, 1)
       auto wait_slot = [&](uint32_t it) {
         return wait_w(bar(ctl.full[it % C::kStages]), (it / C::kStages) & 1);
       };
-      // SS product [M = 128 rows of a] x [N = 128 rows of b]^T over K = D.
+      // SS product [M = 128 rows of a] x [N = 128 rows of b]^T over K = D, four
+      // k-steps per election; a k-step adds its offset (16-byte units) to the
+      // descriptors' address field.
       auto ss = [&](uint32_t d_col, uint32_t a0, uint32_t b0) {
+        const uint64_t da = make_smem_desc(a0, 16, 1024, kSwizzle128B);
+        const uint64_t db = make_smem_desc(b0, 16, 1024, kSwizzle128B);
 #pragma unroll
-        for (int k = 0; k < C::kSSteps; ++k) {
-          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-          mma_f16_ss_w(tmem + d_col, make_smem_desc(a0 + off, 16, 1024, kSwizzle128B),
-                       make_smem_desc(b0 + off, 16, 1024, kSwizzle128B), C::kIdescSS, k > 0);
+        for (int g = 0; g < C::kSSteps / 4; ++g) {
+          const uint64_t o = g * 1024;   // next 128-byte column slab
+          mma_ss_x4_w<false>(tmem + d_col, da + o, da + o + 2, da + o + 4, da + o + 6, db + o,
+                             db + o + 2, db + o + 4, db + o + 6, C::kIdescSS, g > 0 ? 1u : 0u);
         }
       };
       // TS product: A = 128 x 128 bf16 in TMEM, queries [32h, 32h+32) at
       // columns a_col + 32h + [0,16); B = a [queries x D] tile as MN-major operand.
       auto ts = [&](uint32_t d_col, uint32_t a_col, uint32_t b0, bool acc) {
+        const uint64_t db = make_smem_desc(b0, 16384, 1024, kSwizzle128B);
+        const uint32_t ta = tmem + a_col;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t a = tmem + a_col + (k >> 1) * 32 + (k & 1) * 8;
-          mma_f16_ts_w(tmem + d_col, a, make_smem_desc(b0 + k * 2048, 16384, 1024, kSwizzle128B),
-                       C::kIdescTS, (acc || k > 0) ? 1u : 0u);
+        for (int g = 0; g < 2; ++g) {   // k-steps 4g .. 4g+3: A columns 64g + {0, 8, 32, 40}, B rows 2048 bytes apart
+          mma_ts_x4_w<false>(tmem + d_col, ta + 64 * g, ta + 64 * g + 8, ta + 64 * g + 32,
+                             ta + 64 * g + 40, db + 512 * g, db + 512 * g + 128,
+                             db + 512 * g + 256, db + 512 * g + 384, C::kIdescTS,
+                             (acc || g > 0) ? 1u : 0u);
         }
       };
       for (uint32_t k = 0; ok; ++k, ++uit) {
@@ -652,14 +659,30 @@ __global__ void __launch_bounds__(576, 1)
         return wait_w(bar(ctl.full[it % C::kStagesDQ]), (it / C::kStagesDQ) & 1);
       };
       auto slot_addr = [&](uint32_t it) { return sRing + (it % C::kStagesDQ) * C::kTile; };
-      // [128 rows in TMEM at a_col] x [128 rows of the K-major tile b0]^T over K = D
+      // [128 rows in TMEM at a_col] x [128 rows of the K-major tile b0]^T over K = D,
+      // four k-steps per election.
       auto ts_k = [&](uint32_t d_col, uint32_t a_col, uint32_t b0) {
+        const uint64_t db = make_smem_desc(b0, 16, 1024, kSwizzle128B);
+        const uint32_t ta = tmem + a_col;
 #pragma unroll
-        for (int k = 0; k < C::kSSteps; ++k) {
-          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-          mma_f16_ts_w(tmem + d_col, tmem + a_col + 8 * k, make_smem_desc(b0 + off, 16, 1024, kSwizzle128B),
-                       C::kIdescSS, k > 0 ? 1u : 0u);
+        for (int g = 0; g < C::kSSteps / 4; ++g) {
+          const uint64_t o = g * 1024;
+          mma_ts_x4_w<false>(tmem + d_col, ta + 32 * g, ta + 32 * g + 8, ta + 32 * g + 16,
+                             ta + 32 * g + 24, db + o, db + o + 2, db + o + 4, db + o + 6,
+                             C::kIdescSS, g > 0 ? 1u : 0u);
         }
+      };
+      // [128 x 128 bf16 in TMEM at a_col, keys [32h, 32h+32) at columns a_col +
+      // 32h + [0,16)] x [MN-major K tile b0]
+      auto ts_mn = [&](uint32_t d_col, uint32_t a_col, uint32_t b0, bool acc) {
+        const uint64_t db = make_smem_desc(b0, 16384, 1024, kSwizzle128B);
+        const uint32_t ta = tmem + a_col;
+#pragma unroll
+        for (int g = 0; g < 2; ++g)
+          mma_ts_x4_w<false>(tmem + d_col, ta + 64 * g, ta + 64 * g + 8, ta + 64 * g + 32,
+                             ta + 64 * g + 40, db + 512 * g, db + 512 * g + 128,
+                             db + 512 * g + 256, db + 512 * g + 384, C::kIdescTS,
+                             (acc || g > 0) ? 1u : 0u);
       };
       for (uint32_t k = 0; ok; ++k, ++uit) {
         const int u = take_unit(k, ok);
@@ -692,13 +715,7 @@ __global__ void __launch_bounds__(576, 1)
           // dQ += dS K_j once dS is written (over dP)
           if (!(ok = wait_w(bar(ctl.p_ready), gblk & 1))) break;
           tc_fence_after();
-          const uint32_t kb = slot_addr(ik);
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint32_t a = tmem + kColDP + (k >> 1) * 32 + (k & 1) * 8;
-            mma_f16_ts_w(tmem + kColDQ, a, make_smem_desc(kb + k * 2048, 16384, 1024, kSwizzle128B),
-                         C::kIdescTS, (jj > 0 || k > 0) ? 1u : 0u);
-          }
+          ts_mn(kColDQ, kColDP, slot_addr(ik), jj > 0);
           mma_commit_w(bar(ctl.empty[ik % C::kStagesDQ]));   // K_j done
           // dP(jj+1) over dS(jj): after dQ(jj) in issue order
           if (more) {
