@@ -67,12 +67,13 @@ struct BCfg {
   static_assert(D == 64 || D == 128, "head dim 64 or 128");
   static constexpr int kTile = 128 * D * 2;                 // 128 rows x D bf16
   static constexpr int kSlabs = D / 64;                     // 128-byte column slabs
-  // Ring of tiles: dK/dV kernel Q/dO tiles (+ L', D of each Q tile's block);
-  // dQ kernel K/V tiles (its Q and dO live in TMEM, so the ring gets the rest).
-  static constexpr int kStages = (D == 128) ? 4 : 8;
+  // Ring of tiles: dK/dV kernel Q/dO tiles (K, V fixed per unit; L', D come
+  // from global memory); dQ kernel K/V tiles (its Q and dO live in TMEM, so the
+  // ring gets the rest).  Five 32 KB stages at d = 128 (230 KB with K and V):
+  // with four, the next block's Q tile still in flight stalled the MMA warp.
+  static constexpr int kStages = (D == 128) ? 5 : 12;
   static constexpr int kStagesDQ = (D == 128) ? 6 : 12;
-  static constexpr int kStatBytes = 2 * 128 * 4;            // L' and D of one query block
-  static constexpr int kSmemBytes = (2 + kStages) * kTile + kStages * kStatBytes + 1024;
+  static constexpr int kSmemBytes = (2 + kStages) * kTile + 1024;
   static constexpr int kSmemBytesDQ = kStagesDQ * kTile + 1024;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr int kEW = 16;                            // element-wise warps
@@ -160,8 +161,6 @@ __global__ void __launch_bounds__(576, 1)
   const uint32_t sV = sK + C::kTile;
   const uint32_t sRing = sV + C::kTile;     // Q_i / dO_i tiles, alternating
   // L' and D of the query block of the Q item in ring slot s: 128 + 128 floats
-  const uint32_t sStat = sRing + C::kStages * C::kTile;
-  const float* stat = reinterpret_cast<const float*>(smem + (2 + C::kStages) * C::kTile);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   auto bar = [&](uint64_t& b) { return smem_addr(&b); };
@@ -261,15 +260,10 @@ __global__ void __launch_bounds__(576, 1)
           for (int w2 = 0; w2 < 2 && ok; ++w2, ++item) {   // Q_i (+ L', D), then dO_i
             const uint32_t slot = item % C::kStages;
             if (!(ok = wait_bounded(bar(ctl.empty[slot]), ((item / C::kStages) & 1) ^ 1, wc))) break;
-            mbar_arrive_expect_tx(bar(ctl.full[slot]), C::kTile + (w2 == 0 ? C::kStatBytes : 0));
+            mbar_arrive_expect_tx(bar(ctl.full[slot]), C::kTile);
             for (int s = 0; s < C::kSlabs; ++s)
               tma_load_3d_hint(sRing + slot * C::kTile + s * 16384, w2 == 0 ? &tmQ : &tmdO,
                                bar(ctl.full[slot]), s * 64, i * 128, bh, pol_ring);
-            if (w2 == 0) {
-              const size_t off = (size_t)bh * p.Npad + (size_t)i * 128;
-              bulk_load(sStat + slot * C::kStatBytes, p.lp + off, 512, bar(ctl.full[slot]));
-              bulk_load(sStat + slot * C::kStatBytes + 512, p.dd + off, 512, bar(ctl.full[slot]));
-            }
           }
         }
       }
@@ -393,19 +387,33 @@ __global__ void __launch_bounds__(576, 1)
       bwd_qrange(j, p, i_lo, i_hi);
       const int nI = i_hi - i_lo + 1;
       const int key = j * 128 + r;
-      for (int t = 0; t < p.group * nI; ++t, ++gblk, item += 2) {
+      // L' and D of block t's queries 32h + lane, read from global memory one
+      // block ahead (lane i holds query 32h + i; shuffles hand the values to the
+      // other lanes): shared-memory loads queue behind the score products'
+      // operand traffic for hundreds of cycles.
+      const int T = p.group * nI;
+      const int hb = bhk / p.Hk, hg = bhk - hb * p.Hk;
+      auto stat_off = [&](int tt) {
+        const int hh = tt / nI, ii = i_lo + (tt - hh * nI);
+        return (size_t)(hb * p.H + hg * p.group + hh) * p.Npad + (size_t)ii * 128 + 32 * h + lane;
+      };
+      float l_next = 0.0f, d_next = 0.0f;
+      if (T > 0) {
+        l_next = __ldg(p.lp + stat_off(0));
+        d_next = __ldg(p.dd + stat_off(0));
+      }
+      for (int t = 0; t < T; ++t, ++gblk, item += 2) {
         const int i = i_lo + (t - (t / nI) * nI);
+        const float l_lane = l_next, d_lane = d_next;
+        if (t + 1 < T) {
+          l_next = __ldg(p.lp + stat_off(t + 1));
+          d_next = __ldg(p.dd + stat_off(t + 1));
+        }
         const int q0 = i * 128 + 32 * h;   // first query of this thread's columns
         // Mask needed unless every (key, query) of the block is visible.
         const bool full_vis = (!p.causal || j * 128 + 127 <= i * 128) &&
                               (p.window <= 0 || j * 128 > i * 128 + 127 - p.window);
-        // L' and D of this block's queries, staged with the Q tile (item's slot).
-        const float4* Ls4 = reinterpret_cast<const float4*>(stat + (item % C::kStages) * (C::kStatBytes / 4) + 32 * h);
-        const float4* Ds4 = Ls4 + 32;   // D follows L' (128 floats later)
         ok = wait_bounded(bar(ctl.s_full), gblk & 1, wc);
-        // The Q item's slot (with L', D) landed; it is not refilled before this
-        // block's dS^T is signalled, so the phase test is unambiguous.
-        if (ok) ok = wait_bounded(bar(ctl.full[item % C::kStages]), (item / C::kStages) & 1, wc);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;   // a timed-out wait also set the abort flag every other wait honours
         tc_fence_after();
@@ -426,7 +434,10 @@ __global__ void __launch_bounds__(576, 1)
           uint32_t pk[16];
 #pragma unroll
           for (int v4 = 0; v4 < 8; ++v4) {
-            const float4 L = Ls4[v4];
+            const float4 L = make_float4(__shfl_sync(0xffffffffu, l_lane, 4 * v4),
+                                         __shfl_sync(0xffffffffu, l_lane, 4 * v4 + 1),
+                                         __shfl_sync(0xffffffffu, l_lane, 4 * v4 + 2),
+                                         __shfl_sync(0xffffffffu, l_lane, 4 * v4 + 3));
             float a0, a1, a2, a3;
             f32x2_unpack(f32x2_fma(f32x2_pack(__uint_as_float(sv[4 * v4]), __uint_as_float(sv[4 * v4 + 1])), c2,
                                    f32x2_pack(-L.x, -L.y)), a0, a1);
@@ -460,8 +471,10 @@ __global__ void __launch_bounds__(576, 1)
           uint32_t pk[16];
 #pragma unroll
           for (int v4 = 0; v4 < 8; ++v4) {
-            const float4 Dv = Ds4[v4];
-            const float Dd[4] = {Dv.x, Dv.y, Dv.z, Dv.w};
+            const float Dd[4] = {__shfl_sync(0xffffffffu, d_lane, 4 * v4),
+                                 __shfl_sync(0xffffffffu, d_lane, 4 * v4 + 1),
+                                 __shfl_sync(0xffffffffu, d_lane, 4 * v4 + 2),
+                                 __shfl_sync(0xffffffffu, d_lane, 4 * v4 + 3)};
             float ds[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) ds[e] = pr[4 * v4 + e] * (__uint_as_float(dv[4 * v4 + e]) - Dd[e]);
