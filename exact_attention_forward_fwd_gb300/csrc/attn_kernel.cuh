@@ -636,30 +636,30 @@ __global__ void __launch_bounds__(384, 1)
           // 2^tau, as the reference rule requires).  Otherwise (rare after the
           // first block: the block's max is then more than 1 above m) m moves to
           // the block's max, O and the sums are rescaled and the block (still in
-          // TMEM: P has not been stored yet) is taken again.  P is rounded to
+          // registers; P is not signalled yet) is taken again.  P is rounded to
           // bf16 for the PV MMA; the sum of exactly those rounded values (l~)
           // normalises O, so numerator and denominator use the same weights,
           // while the sum of the f32 values (l) gives the logsumexp.
           uint32_t pk[64];
           float e_sum, r_sum;
-          // A row that has seen no visible key yet (every row at a unit's first
-          // block) takes its reference from this block's max before the pass;
-          // its O and sums are still 0, so nothing is rescaled.
-          auto exps = [&](const float (&x)[128]) {
+          // Exponentials of keys [64h, 64h + 64) into P pairs pk[32h, 32h + 32),
+          // with their sums (f32 p and bf16-rounded p).
+          auto exps_half = [&](const float (&x)[128], int h, float& es, float& rs) {
             const float m_use = (m_ref == NEG_INF) ? 0.0f : m_ref;
             const uint64_t c2 = f32x2_pack(cj, cj);
             const uint64_t nm2 = f32x2_pack(-m_use, -m_use);
             uint64_t ex0 = 0, ex1 = 0;   // (0.f, 0.f)
             float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
 #pragma unroll
-            for (int i = 0; i < 64; ++i) {
+            for (int ii = 0; ii < 32; ++ii) {
+              const int i = 32 * h + ii;
               float t0, t1;
               f32x2_unpack(f32x2_fma(f32x2_pack(x[2 * i], x[2 * i + 1]), c2, nm2), t0, t1);
               const float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
               const uint32_t pb = pack_bf16x2(p0, p1);
               pk[i] = pb;
               const uint64_t e = f32x2_pack(p0, p1);
-              if (i & 1) {
+              if (ii & 1) {
                 r2 = add_bf16_lo(pb, r2);
                 r3 = add_bf16_hi(pb, r3);
                 ex1 = f32x2_add(ex1, e);
@@ -671,27 +671,33 @@ __global__ void __launch_bounds__(384, 1)
             }
             float b0, b1;
             f32x2_unpack(f32x2_add(ex0, ex1), b0, b1);
-            e_sum = b0 + b1;
-            r_sum = (r0 + r1) + (r2 + r3);
+            es = b0 + b1;
+            rs = (r0 + r1) + (r2 + r3);
           };
-          {
-            float x[128];
-            load_s(x);
-            // A row that has seen no visible key yet (every row at a unit's
-            // first block) takes its reference from this block's max first; its
-            // O and sums are still 0, so nothing is rescaled.
-            if (!__all_sync(0xffffffffu, m_ref != NEG_INF)) {
-              const float m_blk0 = row_max(x) * cj;
-              if (m_ref == NEG_INF) m_ref = m_blk0;
-            }
-            exps(x);
+          // S stays in registers for the whole block (a retaken block needs no
+          // reload), and P of keys [0, 64) is stored over S columns [0, 32) --
+          // already read -- while the second half's exponentials run; P is
+          // signalled only once the block's sum has passed.  A row with no
+          // visible key yet (every row at a unit's first block) takes its
+          // reference from the block's max first; its O and sums are still 0, so
+          // nothing is rescaled.
+          float x[128];
+          load_s(x);
+          if (!__all_sync(0xffffffffu, m_ref != NEG_INF)) {
+            const float m_blk0 = row_max(x) * cj;
+            if (m_ref == NEG_INF) m_ref = m_blk0;
           }
-          // A sum of 128 terms above 2^tau = 256 has a term above 2; moving m to
+          float es0, rs0, es1, rs1;
+          exps_half(x, 0, es0, rs0);
+          __syncwarp();   // tcgen05.st is warp-collective
+          tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+          exps_half(x, 1, es1, rs1);
+          e_sum = es0 + es1;
+          r_sum = rs0 + rs1;
+          // A sum of 128 terms above 2^8 = 256 has a term above 2; moving m to
           // the block's max makes every term <= 1, so one more pass suffices.
           const bool redo = !(e_sum <= C::kSumLimit);
           if (__any_sync(0xffffffffu, redo)) {
-            float x[128];
-            load_s(x);
             const float m_blk = row_max(x) * cj;
             const float m_new = redo ? fmaxf(m_ref, m_blk) : m_ref;
             const float alpha = redo ? ex2_approx(m_ref - m_new) : 1.0f;
@@ -699,10 +705,14 @@ __global__ void __launch_bounds__(384, 1)
             ell *= alpha;
             ell_r *= alpha;
             m_ref = m_new;
-            exps(x);
+            exps_half(x, 0, es0, rs0);
+            exps_half(x, 1, es1, rs1);
+            e_sum = es0 + es1;
+            r_sum = rs0 + rs1;
+            __syncwarp();
+            tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
           }
           __syncwarp();   // tcgen05.st is warp-collective
-          tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
           tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
           // bf16: one signal for all keys of the block (P·V waits for it once).
           tmem_wait_st();
