@@ -581,14 +581,17 @@ __global__ void __launch_bounds__(384, 1)
           // range.
           uint32_t pk[32];
           float e_sum;
-          auto exps = [&](const float (&x)[128]) {
+          // Exponentials of keys [64hf, 64hf + 64) into pk[16hf, 16hf + 16);
+          // returns their sum of p.
+          auto exps_half = [&](const float (&x)[128], int hf) -> float {
             const float m_use = (m_ref == NEG_INF) ? 0.0f : m_ref;
             const float m_f = m_use - __log2f(v_fold);
             const uint64_t c2 = f32x2_pack(cj, cj);
             const uint64_t nm2 = f32x2_pack(-m_f, -m_f);
             uint64_t s01 = 0, s23 = 0;   // (0.f, 0.f)
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
+            for (int ii = 0; ii < 16; ++ii) {
+              const int i = 16 * hf + ii;
               const int c = 4 * i;
               float t0, t1, t2, t3;
               f32x2_unpack(f32x2_fma(f32x2_pack(x[c], x[c + 1]), c2, nm2), t0, t1);
@@ -601,7 +604,7 @@ __global__ void __launch_bounds__(384, 1)
             }
             float a0, a1;
             f32x2_unpack(f32x2_add(s01, s23), a0, a1);
-            e_sum = (a0 + a1) / v_fold;
+            return (a0 + a1) / v_fold;
           };
           {
             // The block's max first: E4M3 P must never saturate, and with the
@@ -616,17 +619,19 @@ __global__ void __launch_bounds__(384, 1)
             if (jj > 0 && __any_sync(0xffffffffu, need)) rescale_o(alpha);
             ell *= alpha;
             m_ref = m_new;
-            exps(x);
-          }
-          __syncwarp();   // tcgen05.st is warp-collective
-          // keys [64hf, 64hf+64) -> columns [16hf, 16hf+16), one signal each, so
-          // the first half's P.V can start while the second half is stored
+            // keys [64hf, 64hf+64) -> P columns [16hf, 16hf+16), each half
+            // signalled as soon as it is stored, so the first half's P.V runs
+            // during the second half's exponentials.
+            e_sum = 0.0f;
 #pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            tmem_st16(tS + 16 * hf, *reinterpret_cast<uint32_t(*)[16]>(&pk[16 * hf]));
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(bar(ctl.p_ready[t][hf]));
+            for (int hf = 0; hf < 2; ++hf) {
+              e_sum += exps_half(x, hf);
+              __syncwarp();   // tcgen05.st is warp-collective
+              tmem_st16(tS + 16 * hf, *reinterpret_cast<uint32_t(*)[16]>(&pk[16 * hf]));
+              tmem_wait_st();
+              tc_fence_before();
+              mbar_arrive(bar(ctl.p_ready[t][hf]));
+            }
           }
           ell += e_sum;
         } else {
