@@ -466,6 +466,25 @@ def run_mine(args):
     if ga.device_status() != 0:
         raise RuntimeError("kernel status word set during the benchmark")
 
+    # -------------------------------------------------------------- context
+    # torch's scaled_dot_product_attention on the same inputs, timed the same
+    # way: a context number only (whatever backend torch dispatches to), never
+    # a path of this library.
+    context = None
+    if not args.no_extra:
+        import torch.nn.functional as F
+        sdpa = lambda: F.scaled_dot_product_attention(q, k, v, is_causal=w.causal, scale=w.scale)
+        try:
+            for _ in range(args.warmup):
+                sdpa()
+            barrier()
+            ms_sdpa = mor(_time_loop(sdpa, args.steps, stream))
+            context = {"torch_sdpa": {"tflops": w.flops / (ms_sdpa * 1e-3) / 1e12 * ws, "ms": ms_sdpa,
+                                      "torch": torch.__version__, "workload": w.name}}
+        except RuntimeError as e:   # no backend for this device in this torch build
+            context = {"torch_sdpa": {"unavailable": str(e).splitlines()[0][:160]}}
+        barrier()
+
     # ---------------------------------------------------------- CPU baseline
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -498,6 +517,7 @@ def run_mine(args):
             "fp8": fp8,
             "backward": bwd,
             "workloads": others,
+            "context": context,
         }
         print(json.dumps(line))
     if dist is not None:
