@@ -17,9 +17,11 @@
 // Blackwell mapping (this file's own design):
 //   * one persistent CTA per SM; a work unit is (batch*head, pair of 128-row
 //     query tiles); both tiles share every K/V block loaded;
-//   * warps 0-3 / 4-7: softmax of tile 0 / tile 1, one thread per query row,
+//   * warps 0-3 / 4-7: softmax of tile 0 / tile 1, one thread per query row
+//     (224 registers each: warps 8-11 hand theirs over with setmaxnreg),
 //     reading S from tensor memory (TMEM) and writing P back over it;
 //   * warp 8: TMA loads of Q (once per unit) and of K, V blocks into the ring;
+//   * warps 10, 11: no role (they complete the third warpgroup);
 //   * warp 9: allocates TMEM and issues every tcgen05.mma (the warp runs its
 //     loop converged, one elected lane issues):
 //       S_t = Q_t K_j^T  (SS, both operands K-major in shared memory)
@@ -637,8 +639,8 @@ __global__ void __launch_bounds__(384, 1)
         } else {
           // p = 2^(s*c - m) against the running reference max m, so no
           // exponential waits for the block's max.  The block's sum of p bounds
-          // every p in it: if the sum is at most 2^tau the pass stands (p <=
-          // 2^tau, as the reference rule requires).  Otherwise (rare after the
+          // every p in it: if the sum is at most 2^8 the pass stands (p <= 2^8,
+          // as the reference rule requires).  Otherwise (rare after the
           // first block: the block's max is then more than 1 above m) m moves to
           // the block's max, O and the sums are rescaled and the block (still in
           // registers; P is not signalled yet) is taken again.  P is rounded to
