@@ -75,11 +75,12 @@ __global__ void __launch_bounds__(256) fp8_prep_kernel(const uint16_t* __restric
       a[3] = b1 - b3;
 #pragma unroll
       for (int m = 1; m < 32; m <<= 1) {   // half-width 4m across lanes
-        const bool upper = (lane & m) != 0;
+        // lower lane: a + o; upper lane: o - a (one FMA with the lane's sign)
+        const float sgn = (lane & m) ? -1.0f : 1.0f;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float o = __shfl_xor_sync(0xffffffffu, a[e], m);
-          a[e] = upper ? (o - a[e]) : (a[e] + o);
+          a[e] = fmaf(a[e], sgn, o);
         }
       }
 #pragma unroll
@@ -100,13 +101,23 @@ __global__ void __launch_bounds__(256) fp8_prep_kernel(const uint16_t* __restric
   for (int w = 1; w < 8; ++w) bmax = fmaxf(bmax, warp_max[w]);
   const float s = (bmax > 0.f) ? __fdiv_rn(bmax, 448.0f) : 1.0f;
   if (threadIdx.x == 0) scales[(size_t)bh * nblk + blk] = s;
+  // x / s correctly rounded without a division per element: q = RN(x r) with r
+  // the correctly rounded reciprocal, then one correction q + RN(x - q s) r
+  // (the residual is exact by FMA) -- Markstein's final step, which yields the
+  // correctly rounded binary32 quotient when r = RN(1 / s).  The sign is taken
+  // from q so that x = -0 gives -0 (the correction would add +0).
+  const float rcp = __frcp_rn(s);
+  auto div_s = [&](float xv) {
+    const float q = xv * rcp;
+    const float res = fmaf(-q, s, xv);
+    return copysignf(fmaf(res, rcp, q), q);
+  };
 
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const int rl = warp * 16 + i;
     const int r = blk * kRows + rl;
-    const uint32_t code = pack_e4m3x4(__fdiv_rn(v[i][0], s), __fdiv_rn(v[i][1], s),
-                                      __fdiv_rn(v[i][2], s), __fdiv_rn(v[i][3], s));
+    const uint32_t code = pack_e4m3x4(div_s(v[i][0]), div_s(v[i][1]), div_s(v[i][2]), div_s(v[i][3]));
     if (TRANSPOSE) {
       *reinterpret_cast<uint32_t*>(tile + rl * kD + 4 * lane) = code;
     } else if (r < N) {
