@@ -39,7 +39,6 @@ __global__ void __launch_bounds__(256) fp8_prep_kernel(const uint16_t* __restric
                                                        const int8_t* __restrict__ signs, int H,
                                                        int N, int nblk, int Npad) {
   __shared__ float warp_max[8];
-  __shared__ __align__(16) uint8_t tile[TRANSPOSE ? kRows * kD : 16];
   const int blk = blockIdx.x % nblk;
   const int bh = blockIdx.x / nblk;
   const int h = bh % H;
@@ -113,33 +112,38 @@ __global__ void __launch_bounds__(256) fp8_prep_kernel(const uint16_t* __restric
     return copysignf(fmaf(res, rcp, q), q);
   };
 
+  uint32_t cw[16];   // codes of this lane's 4 columns, one word per row
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
-    const int rl = warp * 16 + i;
-    const int r = blk * kRows + rl;
-    const uint32_t code = pack_e4m3x4(div_s(v[i][0]), div_s(v[i][1]), div_s(v[i][2]), div_s(v[i][3]));
-    if (TRANSPOSE) {
-      *reinterpret_cast<uint32_t*>(tile + rl * kD + 4 * lane) = code;
-    } else if (r < N) {
-      *reinterpret_cast<uint32_t*>(x8 + ((size_t)bh * N + r) * kD + 4 * lane) = code;
-    }
+    const int r = blk * kRows + warp * 16 + i;
+    cw[i] = pack_e4m3x4(div_s(v[i][0]), div_s(v[i][1]), div_s(v[i][2]), div_s(v[i][3]));
+    if (!TRANSPOSE && r < N)
+      *reinterpret_cast<uint32_t*>(x8 + ((size_t)bh * N + r) * kD + 4 * lane) = cw[i];
   }
   if (TRANSPOSE) {
-    __syncthreads();
-    // Output row c (a head-dim column) holds this block's 128 keys, contiguous.
-    const int c = threadIdx.x >> 1;
-    const int k0 = (threadIdx.x & 1) * 64;
-    uint32_t w[16];
+    // Output row c (a head-dim column) holds the block's 128 keys, contiguous.
+    // Each 4 x 4 byte block (4 rows x this lane's 4 columns) is transposed in
+    // registers with byte permutes, so the lane owns 16 consecutive keys of
+    // each of its columns: one 16-byte store per column.  Rows past N hold
+    // code 0, the padding.
+    uint32_t col[4][4];   // [column e][group g of 4 rows]
 #pragma unroll
-    for (int q = 0; q < 16; ++q) {
-      uint32_t acc = 0;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc |= static_cast<uint32_t>(tile[(k0 + 4 * q + e) * kD + c]) << (8 * e);
-      w[q] = acc;
+    for (int g = 0; g < 4; ++g) {
+      const uint32_t t0 = __byte_perm(cw[4 * g], cw[4 * g + 1], 0x5140);
+      const uint32_t t1 = __byte_perm(cw[4 * g], cw[4 * g + 1], 0x7362);
+      const uint32_t t2 = __byte_perm(cw[4 * g + 2], cw[4 * g + 3], 0x5140);
+      const uint32_t t3 = __byte_perm(cw[4 * g + 2], cw[4 * g + 3], 0x7362);
+      col[0][g] = __byte_perm(t0, t2, 0x5410);
+      col[1][g] = __byte_perm(t0, t2, 0x7632);
+      col[2][g] = __byte_perm(t1, t3, 0x5410);
+      col[3][g] = __byte_perm(t1, t3, 0x7632);
     }
-    uint4* dst = reinterpret_cast<uint4*>(x8 + ((size_t)bh * kD + c) * Npad + (size_t)blk * kRows + k0);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+    for (int e = 0; e < 4; ++e) {
+      uint4* dst = reinterpret_cast<uint4*>(x8 + ((size_t)bh * kD + 4 * lane + e) * Npad +
+                                            (size_t)blk * kRows + warp * 16);
+      *dst = make_uint4(col[e][0], col[e][1], col[e][2], col[e][3]);
+    }
   }
 }
 
