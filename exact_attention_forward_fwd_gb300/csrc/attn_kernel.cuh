@@ -251,8 +251,10 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(bar(ctl.q_full[t]), 1);
       mbar_init(bar(ctl.q_empty[t]), 1);
       mbar_init(bar(ctl.s_full[t]), 1);
-      mbar_init(bar(ctl.p_ready[t][0]), 128);
-      mbar_init(bar(ctl.p_ready[t][1]), 128);
+      // FP8: one arrival per softmax warp of the tile (measured +1 %); bf16: one
+      // per thread (a warp-level arrival after __syncwarp measured -2 % there).
+      mbar_init(bar(ctl.p_ready[t][0]), FP8 ? 4 : 128);
+      mbar_init(bar(ctl.p_ready[t][1]), FP8 ? 4 : 128);
       mbar_init(bar(ctl.o_final[t]), 1);
     }
     mbar_init(bar(ctl.drain), 1);
@@ -632,7 +634,8 @@ __global__ void __launch_bounds__(384, 1)
               tmem_st16(tS + 16 * hf, *reinterpret_cast<uint32_t(*)[16]>(&pk[16 * hf]));
               tmem_wait_st();
               tc_fence_before();
-              mbar_arrive(bar(ctl.p_ready[t][hf]));
+              __syncwarp();
+              if (lane == 0) mbar_arrive(bar(ctl.p_ready[t][hf]));
             }
           }
           ell += e_sum;
