@@ -79,6 +79,7 @@ AttnParams base_params(void* o, float* lse, int B, int H, int H_kv, int N, float
 }
 
 constexpr int kMaxSplits = 64;
+constexpr long long kUnitOverheadBlocks = 4;   // split-KV time model (measured)
 
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
@@ -229,19 +230,18 @@ int attn_splitkv_default_splits(int B, int H, int N, int num_sms) {
   if (B < 1 || H < 1 || N < 1 || num_sms < 1) return 0;
   const long long units = static_cast<long long>(B) * H * ((N + 255) / 256);
   if (units >= num_sms) return 1;
-  // Fraction of the SM slots of whole waves that the units of S splits fill.
-  auto fill = [&](long long S) {
-    const long long u = units * S;
-    const long long waves = (u + num_sms - 1) / num_sms;
-    return static_cast<double>(u) / static_cast<double>(waves * num_sms);
-  };
+  // Time model in key blocks: waves of units x (blocks per unit + a fixed
+  // per-unit cost of about four blocks: Q load, pipeline fill, epilogue).  The
+  // smallest S with the least modelled time wins.
   const long long blocks = (N + 127) / 128;
   const long long cap = blocks < kMaxSplits ? blocks : kMaxSplits;
+  auto cost = [&](long long S) {
+    const long long waves = (units * S + num_sms - 1) / num_sms;
+    return waves * ((blocks + S - 1) / S + kUnitOverheadBlocks);
+  };
   long long best = 1;
-  for (long long S = 1; S <= cap; ++S) {
-    if (fill(S) >= 0.9) return static_cast<int>(S);
-    if (fill(S) > fill(best)) best = S;
-  }
+  for (long long S = 2; S <= cap; ++S)
+    if (cost(S) < cost(best)) best = S;
   return static_cast<int>(best);
 }
 

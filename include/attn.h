@@ -148,11 +148,13 @@ ATTN_API int attn_fwd_splitkv_static(const void* q, const void* k, const void* v
  * (B, H, N < 1, d not 64 or 128, num_splits outside 1 .. 64).  Host arithmetic. */
 ATTN_API size_t attn_splitkv_workspace_bytes(int B, int H, int N, int d, int num_splits);
 
-/* A split count that fills a device with num_sms SMs: 1 if the plain schedule
- * has at least num_sms units; else the smallest count S (S <= 64 and S <=
- * ceil(N / 128), the number of 128-key blocks) whose units * S work units fill
- * at least 90% of the SM slots of the waves they take, or, if none does, the
- * S that fills them best.  0 for invalid arguments.  Host arithmetic. */
+/* A split count for a device with num_sms SMs: 1 if the plain schedule has at
+ * least num_sms units; else the smallest count S (S <= 64 and S <= ceil(N /
+ * 128), the number of 128-key blocks) that minimises a time model in key
+ * blocks: waves of units * S work units x (ceil(blocks / S) + 4), the 4
+ * standing for a unit's fixed cost (Q load, pipeline fill, epilogue; measured
+ * on the two-head 8192-token workloads).  0 for invalid arguments.  Host
+ * arithmetic. */
 ATTN_API int attn_splitkv_default_splits(int B, int H, int N, int num_sms);
 
 /* Preparation of FP8 E4M3 operands with per-block scales and, optionally,

@@ -114,8 +114,8 @@ def test_product_path_has_no_cpu_fallback():
 def test_splitkv_workspace_and_default_splits(L):
     """Host arithmetic of the split-KV contract: workspace = partial O (f32) and
     partial lse (f32), each rounded up to 256 bytes; the default split count is
-    the smallest that fills >= 90% of the SM slots of its waves (capped by the
-    128-key blocks and by 64), else the best-filling one."""
+    1 when the plain schedule fills the SMs, else the smallest S (capped by the
+    128-key blocks and by 64) minimising waves x (blocks per unit + 4)."""
     def ws(B, H, N, d, S):
         rows = S * B * H * N
         up = lambda x: (x + 255) // 256 * 256
@@ -128,18 +128,15 @@ def test_splitkv_workspace_and_default_splits(L):
         u = B * H * ((N + 255) // 256)
         if u >= sms:
             return 1
-        fill = lambda S: u * S / (-(-u * S // sms) * sms)
-        cap = min(64, (N + 127) // 128)
-        for S in range(1, cap + 1):
-            if fill(S) >= 0.9:
-                return S
-        return max(range(1, cap + 1), key=lambda S: (fill(S), -S))
+        nb = (N + 127) // 128
+        cost = lambda S: (-(-u * S // sms)) * (-(-nb // S) + 4)
+        return min(range(1, min(64, nb) + 1), key=lambda S: (cost(S), S))
     cases = [(2, 16, 8192, 152), (1, 2, 8192, 152), (1, 2, 256, 152), (1, 1, 32768, 152),
              (1, 1, 16384, 1000), (1, 1, 16384, 10000), (3, 1, 1000, 152), (1, 3, 77, 152)]
     for c in cases:
         assert ga.splitkv_default_splits(*c) == expect(*c), c
     assert ga.splitkv_default_splits(2, 16, 8192, 152) == 1      # 1024 units already
-    assert ga.splitkv_default_splits(1, 2, 8192, 152) == 7       # 64 units: 448 of 456 slots
+    assert ga.splitkv_default_splits(1, 2, 8192, 152) == 2       # 64 units: 1 wave of 32-block units
     assert ga.splitkv_default_splits(1, 2, 256, 152) == 2        # capped by 2 key blocks
     assert ga.splitkv_default_splits(1, 1, 16384, 10000) == 64   # capped at 64
     assert ga.splitkv_default_splits(0, 1, 1, 152) == 0
