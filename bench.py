@@ -447,8 +447,8 @@ def run_mine(args):
             others[name] = {"tflops": wo.flops / (mso * 1e-3) / 1e12 * ws, "ms": mso,
                             "l2": "flushed before each launch"}
             if name.startswith("n8192_d128_b1h2"):
-                # Split-KV on the same inputs, with the split count that fills the SMs.
-                S = ga.splitkv_default_splits(wo.B, wo.H, wo.N, sms)
+                # Split-KV on the same inputs, with the library's default split count.
+                S = ga.splitkv_default_splits(wo.B, wo.H, wo.N, wo.d, wo.causal, sms)
                 wsp = torch.empty(ga.splitkv_workspace_bytes(wo.B, wo.H, wo.N, wo.d, S),
                                   dtype=torch.uint8, device=dev)
                 fs = lambda: ga.attn_fwd_splitkv(a, b, c, causal=wo.causal, scale=wo.scale,

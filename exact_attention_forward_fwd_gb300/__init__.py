@@ -12,7 +12,7 @@ Functions mirror the C entry points:
   attn_fwd_ex(q, k, v, causal=False, window=0, scale=None, ...)   (grouped KV heads, window)
   attn_fwd_splitkv(q, k, v, causal=False, window=0, num_splits=None, workspace=None, ...)
   attn_fwd_splitkv_static(q, k, v, causal=False, window=0, num_splits=None, ...)  (no allocation)
-  splitkv_workspace_bytes(B, H, N, d, num_splits), splitkv_default_splits(B, H, N, num_sms)
+  splitkv_workspace_bytes(B, H, N, d, num_splits), splitkv_default_splits(B, H, N, d, causal, num_sms)
   attn_bwd(q, k, v, o, lse, dO, causal=False, window=0, scale=None, ...)  -> (dq, dk, dv)
   bwd_workspace_bytes(B, H, N, d)
   fp8_prep(x, signs=None, transpose=False, out=None, scales=None)
@@ -73,7 +73,7 @@ def lib() -> ctypes.CDLL:
     L.attn_bwd_workspace_bytes.restype = ctypes.c_size_t
     L.attn_splitkv_workspace_bytes.argtypes = [i, i, i, i, i]
     L.attn_splitkv_workspace_bytes.restype = ctypes.c_size_t
-    L.attn_splitkv_default_splits.argtypes = [i, i, i, i]
+    L.attn_splitkv_default_splits.argtypes = [i, i, i, i, i, i]
     L.attn_status_str.argtypes = [i]
     L.attn_status_str.restype = ctypes.c_char_p
     for name in ("attn_fwd", "attn_fwd_ex", "attn_fp8_prep", "attn_fwd_fp8", "attn_fwd_debug",
@@ -193,9 +193,10 @@ def splitkv_workspace_bytes(B: int, H: int, N: int, d: int, num_splits: int) -> 
     return int(lib().attn_splitkv_workspace_bytes(B, H, N, d, num_splits))
 
 
-def splitkv_default_splits(B: int, H: int, N: int, num_sms: int) -> int:
-    """Split count that fills num_sms SMs for this shape (0 for invalid arguments)."""
-    return int(lib().attn_splitkv_default_splits(B, H, N, num_sms))
+def splitkv_default_splits(B: int, H: int, N: int, d: int, causal: bool, num_sms: int) -> int:
+    """Split count the library's time model picks for this shape on num_sms
+    SMs (1 when the plain schedule fills them; 0 for invalid arguments)."""
+    return int(lib().attn_splitkv_default_splits(B, H, N, d, int(bool(causal)), num_sms))
 
 
 def attn_fwd_splitkv(q, k, v, causal: bool = False, window: int = 0, scale: float | None = None,
@@ -219,7 +220,7 @@ def attn_fwd_splitkv(q, k, v, causal: bool = False, window: int = 0, scale: floa
     scale = d ** -0.5 if scale is None else scale
     if num_splits is None:
         sms = torch.cuda.get_device_properties(q.device).multi_processor_count
-        num_splits = splitkv_default_splits(B, H, N, sms)
+        num_splits = splitkv_default_splits(B, H, N, d, causal, sms)
     need = splitkv_workspace_bytes(B, H, N, d, num_splits)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
@@ -260,7 +261,7 @@ def attn_fwd_splitkv_static(q, k, v, causal: bool = False, window: int = 0,
     scale = d ** -0.5 if scale is None else scale
     if num_splits is None:
         sms = torch.cuda.get_device_properties(q.device).multi_processor_count
-        num_splits = splitkv_default_splits(B, H, N, sms)
+        num_splits = splitkv_default_splits(B, H, N, d, causal, sms)
     out = torch.empty_like(q) if out is None else out
     _need(out, "out", torch.bfloat16, q.shape)
     if lse is None and return_lse:

@@ -7,6 +7,10 @@
 #include <cmath>
 #include <cstdint>
 #include <mutex>
+#include <algorithm>
+#include <functional>
+#include <queue>
+#include <vector>
 
 #include "attn.h"
 #include "attn_bwd.cuh"
@@ -80,6 +84,7 @@ AttnParams base_params(void* o, float* lse, int B, int H, int H_kv, int N, float
 
 constexpr int kMaxSplits = 64;
 constexpr long long kUnitOverheadBlocks = 4;   // split-KV time model (measured)
+constexpr double kBytesPerKeyBlock = 8.8e6;     // HBM bytes moved in one key block's time
 
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
@@ -226,22 +231,48 @@ size_t attn_splitkv_workspace_bytes(int B, int H, int N, int d, int num_splits) 
   return splitkv_bytes(B, H, N, d, num_splits, nullptr);
 }
 
-int attn_splitkv_default_splits(int B, int H, int N, int num_sms) {
-  if (B < 1 || H < 1 || N < 1 || num_sms < 1) return 0;
-  const long long units = static_cast<long long>(B) * H * ((N + 255) / 256);
-  if (units >= num_sms) return 1;
-  // Time model in key blocks: waves of units x (blocks per unit + a fixed
-  // per-unit cost of about four blocks: Q load, pipeline fill, epilogue).  The
-  // smallest S with the least modelled time wins.
+int attn_splitkv_default_splits(int B, int H, int N, int d, int causal, int num_sms) {
+  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128) || num_sms < 1) return 0;
+  const long long bh = static_cast<long long>(B) * H;
+  const long long npairs = (N + 255) / 256;
+  if (bh * npairs >= num_sms) return 1;
+  // Time model in key blocks.  The kernel's dynamic scheduler hands out units
+  // in its own order (causal: longest pairs first, split ranges innermost);
+  // each SM takes the next one when it is free, and a unit costs its key
+  // blocks plus a fixed four (Q load, pipeline fill, epilogue) or one if its
+  // range is empty.  S > 1 adds the merge: d floats per row and split
+  // written and read again, one key block's time moving about 8.8 MB.
   const long long blocks = (N + 127) / 128;
   const long long cap = blocks < kMaxSplits ? blocks : kMaxSplits;
-  auto cost = [&](long long S) {
-    const long long waves = (units * S + num_sms - 1) / num_sms;
-    return waves * ((blocks + S - 1) / S + kUnitOverheadBlocks);
+  const double merge_per_split = static_cast<double>(bh) * N * d * 8.0 / kBytesPerKeyBlock;
+  auto model = [&](long long S) {
+    std::priority_queue<long long, std::vector<long long>, std::greater<long long>> free_at;
+    for (int m = 0; m < num_sms; ++m) free_at.push(0);
+    long long span = 0;
+    for (long long r = 0; r < npairs; ++r) {
+      const long long pair = causal ? npairs - 1 - r : r;
+      const long long nb = causal ? std::min(blocks, 2 * pair + 2) : blocks;
+      for (long long h = 0; h < bh; ++h) {
+        for (long long sp = 0; sp < S; ++sp) {
+          const long long sz = (sp + 1) * nb / S - sp * nb / S;
+          const long long t = free_at.top() + (sz > 0 ? sz + kUnitOverheadBlocks : 1);
+          free_at.pop();
+          free_at.push(t);
+          span = std::max(span, t);
+        }
+      }
+    }
+    return static_cast<double>(span) + (S > 1 ? S * merge_per_split : 0.0);
   };
   long long best = 1;
-  for (long long S = 2; S <= cap; ++S)
-    if (cost(S) < cost(best)) best = S;
+  double best_t = model(1);
+  for (long long S = 2; S <= cap; ++S) {
+    const double t = model(S);
+    if (t < best_t) {
+      best = S;
+      best_t = t;
+    }
+  }
   return static_cast<int>(best);
 }
 

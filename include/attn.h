@@ -148,14 +148,19 @@ ATTN_API int attn_fwd_splitkv_static(const void* q, const void* k, const void* v
  * (B, H, N < 1, d not 64 or 128, num_splits outside 1 .. 64).  Host arithmetic. */
 ATTN_API size_t attn_splitkv_workspace_bytes(int B, int H, int N, int d, int num_splits);
 
-/* A split count for a device with num_sms SMs: 1 if the plain schedule has at
- * least num_sms units; else the smallest count S (S <= 64 and S <= ceil(N /
- * 128), the number of 128-key blocks) that minimises a time model in key
- * blocks: waves of units * S work units x (ceil(blocks / S) + 4), the 4
- * standing for a unit's fixed cost (Q load, pipeline fill, epilogue; measured
- * on the two-head 8192-token workloads).  0 for invalid arguments.  Host
+/* A split count for attn_fwd_splitkv on a device with num_sms SMs, for the
+ * shape (B, H, N, d) and causal flag the call will use: 1 if the plain
+ * schedule already has at least num_sms units (pairs of 128-query tiles);
+ * else the smallest S (S <= 64 and S <= ceil(N / 128), the number of 128-key
+ * blocks) that minimises a time model in key blocks.  The model deals the
+ * split units to the SMs in the kernel's own order, each SM taking the next
+ * unit when free (a unit costs its key blocks plus 4 for its fixed work: Q
+ * load, pipeline fill, epilogue), and adds for S > 1 the merge's traffic
+ * (8 bytes per output element and split) at 8.8 MB per key block's time.
+ * The constants were fitted to sweeps of S on the two-head 8192-token
+ * workloads (non-causal and causal).  0 for invalid arguments.  Host
  * arithmetic. */
-ATTN_API int attn_splitkv_default_splits(int B, int H, int N, int num_sms);
+ATTN_API int attn_splitkv_default_splits(int B, int H, int N, int d, int causal, int num_sms);
 
 /* Preparation of FP8 E4M3 operands with per-block scales and, optionally,
  * incoherent processing ("4.3 FlashAttention 2 & 3", section "Incoherent

@@ -115,7 +115,9 @@ def test_splitkv_workspace_and_default_splits(L):
     """Host arithmetic of the split-KV contract: workspace = partial O (f32) and
     partial lse (f32), each rounded up to 256 bytes; the default split count is
     1 when the plain schedule fills the SMs, else the smallest S (capped by the
-    128-key blocks and by 64) minimising waves x (blocks per unit + 4)."""
+    128-key blocks and by 64) minimising the finish time of the split units
+    dealt in the kernel's order to the first free SM (blocks + 4 per unit, 1
+    for an empty range) plus, for S > 1, S x B*H*N*d*8 / 8.8e6 for the merge."""
     def ws(B, H, N, d, S):
         rows = S * B * H * N
         up = lambda x: (x + 255) // 256 * 256
@@ -124,22 +126,38 @@ def test_splitkv_workspace_and_default_splits(L):
         assert ga.splitkv_workspace_bytes(*args) == ws(*args), args
     for bad in [(0, 1, 1, 64, 1), (1, 1, 1, 96, 1), (1, 1, 1, 64, 0), (1, 1, 1, 64, 65)]:
         assert ga.splitkv_workspace_bytes(*bad) == 0, bad
-    def expect(B, H, N, sms):
-        u = B * H * ((N + 255) // 256)
-        if u >= sms:
+
+    def finish(B, H, N, causal, S, sms):
+        # plain list scheduling, SM loads kept as a sorted list
+        npairs, nb_all = (N + 255) // 256, (N + 127) // 128
+        pairs = range(npairs - 1, -1, -1) if causal else range(npairs)
+        loads = [0] * sms
+        for pr in pairs:
+            nb = min(nb_all, 2 * pr + 2) if causal else nb_all
+            for _ in range(B * H):
+                for sp in range(S):
+                    size = (sp + 1) * nb // S - sp * nb // S
+                    loads[0] += size + 4 if size else 1
+                    loads.sort()
+        return max(loads)
+
+    def expect(B, H, N, d, causal, sms):
+        if B * H * ((N + 255) // 256) >= sms:
             return 1
         nb = (N + 127) // 128
-        cost = lambda S: (-(-u * S // sms)) * (-(-nb // S) + 4)
-        return min(range(1, min(64, nb) + 1), key=lambda S: (cost(S), S))
-    cases = [(2, 16, 8192, 152), (1, 2, 8192, 152), (1, 2, 256, 152), (1, 1, 32768, 152),
-             (1, 1, 16384, 1000), (1, 1, 16384, 10000), (3, 1, 1000, 152), (1, 3, 77, 152)]
+        t = lambda S: finish(B, H, N, causal, S, sms) + (S * B * H * N * d * 8 / 8.8e6 if S > 1 else 0)
+        return min(range(1, min(64, nb) + 1), key=lambda S: (t(S), S))
+    cases = [(2, 16, 8192, 128, 0, 152), (1, 2, 8192, 128, 0, 152), (1, 2, 8192, 128, 1, 152),
+             (1, 2, 256, 64, 0, 152), (1, 1, 32768, 64, 1, 152), (1, 1, 16384, 128, 0, 1000),
+             (3, 1, 1000, 64, 1, 152), (1, 3, 77, 128, 0, 152), (1, 4, 4096, 128, 1, 132)]
     for c in cases:
         assert ga.splitkv_default_splits(*c) == expect(*c), c
-    assert ga.splitkv_default_splits(2, 16, 8192, 152) == 1      # 1024 units already
-    assert ga.splitkv_default_splits(1, 2, 8192, 152) == 2       # 64 units: 1 wave of 32-block units
-    assert ga.splitkv_default_splits(1, 2, 256, 152) == 2        # capped by 2 key blocks
-    assert ga.splitkv_default_splits(1, 1, 16384, 10000) == 64   # capped at 64
-    assert ga.splitkv_default_splits(0, 1, 1, 152) == 0
+    assert ga.splitkv_default_splits(2, 16, 8192, 128, 0, 152) == 1   # 1024 units already
+    assert ga.splitkv_default_splits(1, 2, 8192, 128, 0, 152) == 2    # 64 units: 1 wave of 32-block units
+    assert ga.splitkv_default_splits(1, 2, 8192, 128, 1, 152) == 4    # causal: shorter units pack tighter
+    assert ga.splitkv_default_splits(1, 2, 256, 64, 0, 152) == 2      # capped by 2 key blocks
+    assert ga.splitkv_default_splits(0, 1, 1, 128, 0, 152) == 0
+    assert ga.splitkv_default_splits(1, 1, 1, 96, 0, 152) == 0        # head dim 64 or 128 only
 
 
 def test_splitkv_validation_codes(L):

@@ -78,12 +78,12 @@ def test_grouped_heads_and_window(H_kv, window, splits):
 
 @pytest.mark.parametrize("name", ["n8192_d128_b1h2", "n8192_d128_b1h2_causal"])
 def test_workload_sampled_rows_default_splits(name):
-    """The one-sequence, two-head 8192-token workload with the split count that
-    fills the device (the benchmark's launch configuration)."""
+    """The one-sequence, two-head 8192-token workload with the library's default
+    split count (the benchmark's launch configuration)."""
     w = inputs.WORKLOADS[name]
     q, k, v = inputs.workload_inputs(w)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    splits = ga.splitkv_default_splits(w.B, w.H, w.N, sms)
+    splits = ga.splitkv_default_splits(w.B, w.H, w.N, w.d, w.causal, sms)
     assert splits > 1
     rows = inputs.sample_rows(w.N, 64, w.seed)
     m = _run(q, k, v, w.causal, splits, rows=rows, scale=w.scale)
