@@ -152,11 +152,12 @@ int run_bf16(const void* q, const void* k, const void* v, void* o, float* lse, i
   int sms = 0;
   if ((rc = device_check(&sms))) return rc;
   const int BH = B * H, BHk = B * H_kv;
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   const uint32_t box_inner = 64;   // 128-byte rows of the swizzle atom
   if (!encode_map_3d(&mq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, N, BH, box_inner, 128) ||
       !encode_map_3d(&mk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, N, BHk, box_inner, 128) ||
-      !encode_map_3d(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, N, BHk, box_inner, 128))
+      !encode_map_3d(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, N, BHk, box_inner, 128) ||
+      !encode_map_3d(&mo, o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, N, BH, box_inner, 32))
     return ATTN_ERR_CUDA;
   AttnParams p = base_params(o, lse, B, H, H_kv, N, scale, causal, window);
   p.status = status;
@@ -169,8 +170,8 @@ int run_bf16(const void* q, const void* k, const void* v, void* o, float* lse, i
     p.lse_part = reinterpret_cast<float*>(static_cast<char*>(split.workspace) + lse_off);
   }
   const int grid = p.num_units < sms ? p.num_units : sms;
-  cudaError_t e = (d == 64) ? launch_attn_bf16_d64(mq, mk, mv, p, grid, stream)
-                            : launch_attn_bf16_d128(mq, mk, mv, p, grid, stream);
+  cudaError_t e = (d == 64) ? launch_attn_bf16_d64(mq, mk, mv, mo, p, grid, stream)
+                            : launch_attn_bf16_d128(mq, mk, mv, mo, p, grid, stream);
   if (e == cudaSuccess && split.splits != 0)
     e = launch_splitkv_merge(p.o_part, p.lse_part, o, lse, split.splits, BH, N, d, stream);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
@@ -377,17 +378,18 @@ int attn_fwd_fp8(const void* q8, const void* k8, const void* v8t, const float* q
   if ((rc = device_check(&sms))) return rc;
   const int BH = B * H;
   const int Npad = ((N + 127) / 128) * 128;
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   if (!encode_map_3d(&mq, q8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, d, N, BH, 128, 128) ||
       !encode_map_3d(&mk, k8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, d, N, BH, 128, 128) ||
-      !encode_map_3d(&mv, v8t, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Npad, d, BH, 128, 128))
+      !encode_map_3d(&mv, v8t, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Npad, d, BH, 128, 128) ||
+      !encode_map_3d(&mo, o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, N, BH, 64, 32))
     return ATTN_ERR_CUDA;
   AttnParams p = base_params(o, lse, B, H, H, N, scale, causal, 0);
   p.q_scale = q_scale;
   p.k_scale = k_scale;
   p.v_scale = v_scale;
   const int grid = p.num_units < sms ? p.num_units : sms;
-  cudaError_t e = launch_attn_fp8_d128(mq, mk, mv, p, grid, reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_attn_fp8_d128(mq, mk, mv, mo, p, grid, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

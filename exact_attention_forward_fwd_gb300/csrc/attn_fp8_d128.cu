@@ -5,8 +5,8 @@
 namespace gb300 {
 
 cudaError_t launch_attn_fp8_d128(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                           const AttnParams& p, int grid, cudaStream_t stream) {
-  return launch_attn<128, true>(q, k, v, p, grid, stream);
+                                 const CUtensorMap& o, const AttnParams& p, int grid, cudaStream_t stream) {
+  return launch_attn<128, true>(q, k, v, o, p, grid, stream);
 }
 
 int status_attn_fp8_d128(bool clear) { return read_tu_status(clear); }

@@ -105,7 +105,8 @@ struct KCfg {
   static constexpr int kSlabs = kRowBytes / 128;           // 128-byte column slabs per tile
   static constexpr int kTileBytes = 128 * kRowBytes;       // 128-row tile (V / V^T tile the same)
   static constexpr int kStages = (kTileBytes == 32768) ? 4 : 8;
-  static constexpr int kSmemBytes = (2 + kStages) * kTileBytes + 1024;
+  static constexpr int kOStageBytes = D == 128 ? 16384 : 0;   // per tile: 4 warps x 32 rows x 64 bf16 of O
+  static constexpr int kSmemBytes = (2 + kStages) * kTileBytes + 2 * kOStageBytes + 1024;
   static constexpr uint32_t kTmemCols = 512;
   // 12 warps: two softmax warpgroups (warps 0-7), then load (8), MMA (9) and
   // two idle warps (10, 11) that complete the third warpgroup so that it can
@@ -229,7 +230,8 @@ __device__ __forceinline__ Unit unit_of(int u, const AttnParams& p) {
 template <int D, bool FP8>
 __global__ void __launch_bounds__(384, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                    const AttnParams p) {
   using C = KCfg<D, FP8>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ SmemCtl ctl;
@@ -237,6 +239,7 @@ __global__ void __launch_bounds__(384, 1)
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sQ = smem_addr(smem);                         // Q tile 0, Q tile 1
   const uint32_t sKV = sQ + 2 * C::kTileBytes;                 // ring of K / V tiles
+  const uint32_t sO = sKV + C::kStages * C::kTileBytes;        // O staging (d = 128), 4 KB per softmax warp
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
@@ -320,6 +323,20 @@ __global__ void __launch_bounds__(384, 1)
         if (u < 0) break;
         const Unit w = unit_of(u, p);
         if (w.nblocks == 0) continue;   // empty key range (split-KV)
+        // Warm L2 with this unit's Q tiles and first two key blocks while the
+        // previous unit still runs: their loads wait for its buffers, and would
+        // otherwise start at HBM latency then.
+        for (int t = 0; t < 2 && w.pair * 256 + t * 128 < p.N; ++t)
+          for (int s = 0; s < C::kSlabs; ++s)
+            tma_prefetch_3d(&tmQ, s * (FP8 ? 128 : 64), w.pair * 256 + t * 128, w.bh);
+        for (int jj = 0; jj < 2 && jj < w.nblocks; ++jj) {
+          const int j = w.j0 + jj;
+          for (int s = 0; s < C::kSlabs; ++s) {
+            tma_prefetch_3d(&tmK, s * (FP8 ? 128 : 64), j * 128, w.bhk);
+            if (!FP8) tma_prefetch_3d(&tmV, s * 64, j * 128, w.bhk);
+          }
+          if (FP8) tma_prefetch_3d(&tmV, j * 128, 0, w.bhk);
+        }
         for (int t = 0; t < 2 && ok; ++t) {
           if (uit > 0) ok = wait_bounded(bar(ctl.q_empty[t]), (uit - 1) & 1, wc);
           if (!ok) break;
@@ -492,6 +509,26 @@ __global__ void __launch_bounds__(384, 1)
     const float NEG_INF = __int_as_float(0xff800000);
     uint32_t sit = 0, uit = 0;
     bool ok = true;
+    // 64 columns of this thread's row of O_t from TMEM, times inv, as bf16 pairs.
+    auto load_o_bf16 = [&](int col, float inv_o, uint32_t (&pk)[32]) {
+      uint32_t ov[64];
+      __syncwarp();
+      tmem_ld32(tO + col, *reinterpret_cast<uint32_t(*)[32]>(&ov[0]));
+      tmem_ld32(tO + col + 32, *reinterpret_cast<uint32_t(*)[32]>(&ov[32]));
+      tmem_wait_ld();
+      reg_fence(ov);
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        pk[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv_o, __uint_as_float(ov[2 * i + 1]) * inv_o);
+    };
+    // Row i of a staging buffer (128 bytes at addr) in the 128-byte swizzle.
+    auto stage_row = [&](uint32_t addr, int i, const uint32_t (&pk)[32]) {
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        st_shared_v4(addr + ((c ^ (i & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      fence_proxy_async_smem();   // generic-proxy writes -> the tensor copy's reads
+      __syncwarp();
+    };
     for (uint32_t k = 0; ok; ++k) {
       const int u = take_unit(k, ok);
       if (u < 0) break;
@@ -766,22 +803,40 @@ __global__ void __launch_bounds__(384, 1)
         }
         if (live) p.lse_part[prow] = l2e;
       } else {
-        uint16_t* orow_g = reinterpret_cast<uint16_t*>(p.o) + ((size_t)w.bh * p.N + row) * D;
+        // O_t in bf16 through shared memory: each thread writes its row of a
+        // 64-column slab into a staging buffer in the 128-byte swizzled layout
+        // of the O tensor map (row i at 128 i, 16-byte chunk c at position
+        // c ^ (i & 7): conflict-free), and one lane stores the buffer with a
+        // tensor copy (rows past N are clipped).  Full lines reach L2 and the
+        // warps go on while the copy drains; a buffer is written again only
+        // after the copy out of it has read it.
+        // Each warp stages and stores its own 32 rows (4 KB buffers), so that
+        // no warp waits on another.
+        if constexpr (D == 128) {
+          const uint32_t wstage = sO + t * C::kOStageBytes + wq * 4096;
+          const int wrow0 = w.pair * 256 + t * 128 + wq * 32;
 #pragma unroll 1
-        for (int cc = 0; cc < D; cc += 32) {
-          uint32_t ov[32];
-          __syncwarp();
-          tmem_ld32(tO + cc, ov);
-          tmem_wait_ld();
-          reg_fence(ov);
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            pk[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv, __uint_as_float(ov[2 * i + 1]) * inv);
+          for (int sl = 0; sl < 2; ++sl) {
+            uint32_t pk[32];
+            load_o_bf16(64 * sl, inv, pk);
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+            stage_row(wstage + lane * 128, lane, pk);
+            if (lane == 0 && wrow0 < p.N) {
+              tma_store_3d(&tmO, wstage, 64 * sl, wrow0, w.bh);
+              bulk_commit();
+            }
+          }
+        } else {
+          // d = 64: each thread stores its 128-byte row directly (staging it
+          // measured slower here).
+          uint32_t pk[32];
+          load_o_bf16(0, inv, pk);
           if (live) {
-            uint4* dst = reinterpret_cast<uint4*>(orow_g + cc);
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.o) +
+                                                  ((size_t)w.bh * p.N + row) * D);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            for (int i = 0; i < 8; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
           }
         }
         if (live && p.lse != nullptr) p.lse[(size_t)w.bh * p.N + row] = l2e;
@@ -789,6 +844,8 @@ __global__ void __launch_bounds__(384, 1)
       ++uit;
       // The next unit's first P arrive (after this epilogue) releases O_t.
     }
+    // The staging buffers must outlive every copy out of them.
+    if (D == 128 && lane == 0) bulk_wait_all();
   } else {
     regs_dec<C::kRegsOther>();   // warps 10, 11: no role
   }
@@ -836,7 +893,7 @@ static cudaError_t unit_counter(cudaStream_t stream, int** out) {
 
 template <int D, bool FP8>
 cudaError_t launch_attn(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                        const AttnParams& p, int grid, cudaStream_t stream) {
+                        const CUtensorMap& o, const AttnParams& p, int grid, cudaStream_t stream) {
   using C = KCfg<D, FP8>;
   auto kern = attn_fwd_kernel<D, FP8>;
   cudaError_t e =
@@ -855,7 +912,7 @@ cudaError_t launch_attn(const CUtensorMap& q, const CUtensorMap& k, const CUtens
   cfg.blockDim = dim3(C::kThreads);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = stream;
-  return cudaLaunchKernelEx(&cfg, kern, q, k, v, pd);
+  return cudaLaunchKernelEx(&cfg, kern, q, k, v, o, pd);
 }
 
 // Status word of this translation unit's kernels.

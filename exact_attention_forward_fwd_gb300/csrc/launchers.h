@@ -8,11 +8,11 @@ namespace gb300 {
 
 struct AttnParams;
 
-cudaError_t launch_attn_bf16_d64(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+cudaError_t launch_attn_bf16_d64(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
                                  const AttnParams&, int grid, cudaStream_t);
-cudaError_t launch_attn_bf16_d128(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+cudaError_t launch_attn_bf16_d128(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
                                   const AttnParams&, int grid, cudaStream_t);
-cudaError_t launch_attn_fp8_d128(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+cudaError_t launch_attn_fp8_d128(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
                                  const AttnParams&, int grid, cudaStream_t);
 int status_attn_bf16_d64(bool clear);
 int status_attn_bf16_d128(bool clear);
