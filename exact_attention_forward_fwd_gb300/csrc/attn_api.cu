@@ -168,6 +168,11 @@ int run_bf16(const void* q, const void* k, const void* v, void* o, float* lse, i
     p.num_units *= split.splits;
     p.o_part = static_cast<float*>(split.workspace);
     p.lse_part = reinterpret_cast<float*>(static_cast<char*>(split.workspace) + lse_off);
+    // The kernel stores partial O (f32 [splits * B * H][N][d]) through the O
+    // map in 32-row x 32-column boxes; the merge writes O itself.
+    if (!encode_map_3d(&mo, p.o_part, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, N,
+                       static_cast<uint64_t>(split.splits) * BH, 32, 32))
+      return ATTN_ERR_CUDA;
   }
   const int grid = p.num_units < sms ? p.num_units : sms;
   cudaError_t e = (d == 64) ? launch_attn_bf16_d64(mq, mk, mv, mo, p, grid, stream)

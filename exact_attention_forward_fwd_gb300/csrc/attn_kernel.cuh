@@ -786,6 +786,10 @@ __global__ void __launch_bounds__(384, 1)
         // Split-KV: this key range's O (normalised by its own sum) in fp32.
         const size_t prow = ((size_t)w.split * p.BH + w.bh) * p.N + row;
         float* orow_p = p.o_part + prow * D;
+        // d = 128: staged per warp like the bf16 epilogue below, in 32-column
+        // boxes (32 rows x 128 bytes) of the f32 partial-O tensor map.
+        const uint32_t wstage = sO + t * C::kOStageBytes + wq * 4096;
+        const int wrow0 = w.pair * 256 + t * 128 + wq * 32;
 #pragma unroll 1
         for (int cc = 0; cc < D; cc += 32) {
           uint32_t ov[32];
@@ -793,7 +797,22 @@ __global__ void __launch_bounds__(384, 1)
           tmem_ld32(tO + cc, ov);
           tmem_wait_ld();
           reg_fence(ov);
-          if (live) {
+          if constexpr (D == 128) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * inv);
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              st_shared_v4(wstage + lane * 128 + ((c ^ (lane & 7)) << 4), ov[4 * c], ov[4 * c + 1],
+                           ov[4 * c + 2], ov[4 * c + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0 && wrow0 < p.N) {
+              tma_store_3d(&tmO, wstage, cc, wrow0, w.split * p.BH + w.bh);
+              bulk_commit();
+            }
+          } else if (live) {
             float4* dst = reinterpret_cast<float4*>(orow_p + cc);
 #pragma unroll
             for (int i = 0; i < 8; ++i)
