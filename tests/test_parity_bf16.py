@@ -163,3 +163,44 @@ def test_window_of_n_equals_plain_causal():
     o2, l2 = ga.attn_fwd_ex(q, k, v, causal=True, window=600)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N", [1, 200, 300])
+def test_writes_stay_inside_outputs(N, d):
+    """O (written by tensor stores at d = 128, clipped at N) and lse placed inside
+    larger buffers filled with a sentinel: nothing outside them changes, and the
+    result equals the plain call's."""
+    B, H, pad = 2, 3, 4096
+    q, k, v = (t.cuda() for t in inputs.make_qkv(B, H, N, d, seed=31))
+    n = B * H * N * d
+    sentinel_bits = 0x7E55   # a NaN bit pattern the kernel never writes
+    obuf = torch.full((n + 2 * pad,), sentinel_bits, dtype=torch.int16, device="cuda")
+    lbuf = torch.full((B * H * N + 2 * pad,), -7.25, dtype=torch.float32, device="cuda")
+    o = obuf[pad:pad + n].view(torch.bfloat16).view(B, H, N, d)
+    lse = lbuf[pad:pad + B * H * N].view(B, H, N)
+    for causal in (False, True):
+        ga.attn_fwd(q, k, v, causal=causal, out=o, lse=lse)
+        o_ref, l_ref = ga.attn_fwd(q, k, v, causal=causal)
+        torch.cuda.synchronize()
+        assert ga.device_status() == 0
+        assert torch.equal(o, o_ref) and torch.equal(lse, l_ref)
+        assert bool((obuf[:pad] == sentinel_bits).all()) and bool((obuf[pad + n:] == sentinel_bits).all())
+        assert bool((lbuf[:pad] == -7.25).all()) and bool((lbuf[pad + B * H * N:] == -7.25).all())
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_splitkv_writes_stay_inside_workspace(d):
+    """Split-KV partial results (tensor stores at d = 128) stay inside the bytes
+    splitkv_workspace_bytes reports: the rest of a larger workspace keeps its fill."""
+    B, H, N, S = 1, 3, 300, 3
+    q, k, v = (t.cuda() for t in inputs.make_qkv(B, H, N, d, seed=32))
+    need = ga.splitkv_workspace_bytes(B, H, N, d, S)
+    ws = torch.full((need + 65536,), 0x5A, dtype=torch.uint8, device="cuda")
+    o, lse = ga.attn_fwd_splitkv(q, k, v, causal=True, num_splits=S, workspace=ws)
+    o_ref, l_ref = ga.attn_fwd(q, k, v, causal=True)
+    torch.cuda.synchronize()
+    assert ga.device_status() == 0
+    assert bool((ws[need:] == 0x5A).all())
+    assert (o.float() - o_ref.float()).abs().max().item() < 2e-2
+    assert (lse - l_ref).abs().max().item() < 1e-3

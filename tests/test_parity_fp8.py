@@ -147,3 +147,24 @@ def test_fp8_attention_workload_sampled_rows():
     print(f"fp8 workload ({len(rows)} rows): vs exact {m}; vs quantised operands {mq}")
     assert_fp8_parity(m, w.name)
     assert_fp8_fidelity(mq, w.name)
+
+
+def test_fp8_writes_stay_inside_outputs():
+    """The FP8 kernel's O (tensor stores, clipped at N) inside a larger buffer
+    filled with a sentinel: nothing outside it changes, and the result equals
+    the plain call's."""
+    B, H, N, d, pad = 2, 2, 300, 128, 4096
+    q, k, v = (t.cuda() for t in inputs.make_qkv(B, H, N, d, seed=33))
+    signs = inputs.make_signs(H, d, 33).cuda()
+    q8, sq = ga.fp8_prep(q, signs)
+    k8, sk = ga.fp8_prep(k, signs)
+    v8, sv = ga.fp8_prep(v, None, transpose=True)
+    n = B * H * N * d
+    obuf = torch.full((n + 2 * pad,), 0x7E55, dtype=torch.int16, device="cuda")
+    o = obuf[pad:pad + n].view(torch.bfloat16).view(B, H, N, d)
+    ga.attn_fwd_fp8(q8, k8, v8, sq, sk, sv, causal=True, out=o)
+    o_ref, _ = ga.attn_fwd_fp8(q8, k8, v8, sq, sk, sv, causal=True)
+    torch.cuda.synchronize()
+    assert ga.device_status() == 0
+    assert torch.equal(o, o_ref)
+    assert bool((obuf[:pad] == 0x7E55).all()) and bool((obuf[pad + n:] == 0x7E55).all())
