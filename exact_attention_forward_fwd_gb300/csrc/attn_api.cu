@@ -6,7 +6,6 @@
 
 #include <cmath>
 #include <cstdint>
-#include <mutex>
 #include <algorithm>
 #include <functional>
 #include <queue>
@@ -52,6 +51,18 @@ int check_shape(int B, int H, int N, float scale, int causal) {
   return ATTN_OK;
 }
 
+// The kernels' form of the caller's scale: a positive multiplier of the
+// scores in base 2, |scale| * log2(e), plus two flags.  scale < 0: the score
+// product negates its K operand (exact), so scale * q.k = |scale| * (q.(-k)).
+// scale = 0: every visible score is replaced by 0 (the multiplier is then
+// log2(e), which 0 leaves 0), while masked keys stay -inf.
+void set_scale(float scale, float* scale_log2, int* neg, int* zero) {
+  const double a = scale < 0.0f ? -static_cast<double>(scale) : static_cast<double>(scale);
+  *neg = scale < 0.0f ? 1 : 0;
+  *zero = scale == 0.0f ? 1 : 0;
+  *scale_log2 = static_cast<float>((scale == 0.0f ? 1.0 : a) * 1.4426950408889634);
+}
+
 AttnParams base_params(void* o, float* lse, int B, int H, int H_kv, int N, float scale,
                        int causal, int window) {
   AttnParams p{};
@@ -67,7 +78,7 @@ AttnParams base_params(void* o, float* lse, int B, int H, int H_kv, int N, float
   p.npairs = (N + 255) / 256;
   p.num_units = BH * p.npairs;
   p.causal = causal;
-  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  set_scale(scale, &p.scale_log2, &p.neg_scale, &p.zero_scale);
   p.timeout_ns = kDefaultTimeoutNs;
   p.splits = 1;
   // Causal order: groups of heads whose K and V (bf16, head dim <= 128) take at
@@ -105,25 +116,20 @@ struct SplitArgs {
 
 // Scratch of attn_fwd_splitkv_static: a file-scope device array (no allocation
 // call anywhere).  In host code g_splitkv_scratch names a host-side shadow, not
-// device memory, so the device address is looked up with cudaGetSymbolAddress
-// once per device (with that device current) and that address is what the
-// kernels get.  Every call shares the array; calls that overlap on the GPU race.
+// device memory, so the device address is looked up with cudaGetSymbolAddress,
+// with the calling device current, and that address is what the kernels get.
+// The lookup is repeated on every call (a host-side table lookup once the
+// module is loaded): a cached address would outlive a context torn down and
+// created again.  Every call shares the array; calls that overlap on the GPU
+// race.
 constexpr size_t kStaticScratchBytes = size_t(64) << 20;
 static __device__ __align__(256) unsigned char g_splitkv_scratch[kStaticScratchBytes];
-std::mutex g_scratch_mu;
-void* g_scratch_addr[64] = {};
 
 int static_scratch(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ATTN_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_addr[dev] == nullptr) {
-    void* a = nullptr;
-    if (cudaGetSymbolAddress(&a, g_splitkv_scratch) != cudaSuccess || a == nullptr)
-      return ATTN_ERR_CUDA;
-    g_scratch_addr[dev] = a;
-  }
-  *out = g_scratch_addr[dev];
+  void* a = nullptr;
+  if (cudaGetSymbolAddress(&a, g_splitkv_scratch) != cudaSuccess || a == nullptr)
+    return ATTN_ERR_CUDA;
+  *out = a;
   return ATTN_OK;
 }
 
@@ -336,7 +342,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   p.causal = causal;
   p.nb = (N + 127) / 128;
   p.scale = scale;
-  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  set_scale(scale, &p.scale_log2, &p.neg_scale, &p.zero_scale);
   p.timeout_ns = kDefaultTimeoutNs;
   cudaError_t e = launch_attn_bwd(d, mq, mk, mv, mdo, p, o, dO, lse, lp, dd, sms,
                                   reinterpret_cast<cudaStream_t>(stream));

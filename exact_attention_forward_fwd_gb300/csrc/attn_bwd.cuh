@@ -57,8 +57,10 @@ struct BwdParams {
   int num_units;
   int hgroup;            // causal order: heads per group (their streamed tiles stay in L2)
   int* sched;            // unit counter for dynamic scheduling (zeroed before launch), or null
-  float scale_log2;      // scale * log2(e)
-  float scale;
+  float scale_log2;      // |scale| * log2(e) (log2(e) when scale = 0)
+  int neg_scale;         // scale < 0: the score products negate their B operand
+  int zero_scale;        // scale = 0: every visible score is 0
+  float scale;           // signed: multiplies dQ and dK
   unsigned long long timeout_ns;
 };
 
@@ -291,14 +293,16 @@ __global__ void __launch_bounds__(576, 1)
       // SS product [M = 128 rows of a] x [N = 128 rows of b]^T over K = D, four
       // k-steps per election; a k-step adds its offset (16-byte units) to the
       // descriptors' address field.
-      auto ss = [&](uint32_t d_col, uint32_t a0, uint32_t b0) {
+      // S^T = K Q^T negates Q (its B operand) for a negative scale; dP^T does not.
+      const uint32_t idesc_s = C::kIdescSS | (p.neg_scale ? kIdescNegateB : 0u);
+      auto ss = [&](uint32_t d_col, uint32_t a0, uint32_t b0, uint32_t idesc) {
         const uint64_t da = make_smem_desc(a0, 16, 1024, kSwizzle128B);
         const uint64_t db = make_smem_desc(b0, 16, 1024, kSwizzle128B);
 #pragma unroll
         for (int g = 0; g < C::kSSteps / 4; ++g) {
           const uint64_t o = g * 1024;   // next 128-byte column slab
           mma_ss_x4_w<false>(tmem + d_col, da + o, da + o + 2, da + o + 4, da + o + 6, db + o,
-                             db + o + 2, db + o + 4, db + o + 6, C::kIdescSS, g > 0 ? 1u : 0u);
+                             db + o + 2, db + o + 4, db + o + 6, idesc, g > 0 ? 1u : 0u);
         }
       };
       // TS product: A = 128 x 128 bf16 in TMEM, queries [32h, 32h+32) at
@@ -329,9 +333,9 @@ __global__ void __launch_bounds__(576, 1)
         // prologue: S^T(0), dP^T(0)
         if (!(ok = wait_slot(base) && wait_slot(base + 1))) break;
         tc_fence_after();
-        ss(0, sK, sRing + (base % C::kStages) * C::kTile);
+        ss(0, sK, sRing + (base % C::kStages) * C::kTile, idesc_s);
         mma_commit_w(bar(ctl.s_full));
-        ss(128, sV, sRing + ((base + 1) % C::kStages) * C::kTile);
+        ss(128, sV, sRing + ((base + 1) % C::kStages) * C::kTile, C::kIdescSS);
         mma_commit_w(bar(ctl.dp_full));
         for (int t = 0; t < T && ok; ++t, ++gblk) {
           const uint32_t iq = base + 2 * t, io = iq + 1;
@@ -347,7 +351,7 @@ __global__ void __launch_bounds__(576, 1)
           if (more) {
             if (!(ok = wait_slot(iq + 2))) break;
             tc_fence_after();
-            ss(0, sK, sRing + ((iq + 2) % C::kStages) * C::kTile);
+            ss(0, sK, sRing + ((iq + 2) % C::kStages) * C::kTile, idesc_s);
             mma_commit_w(bar(ctl.s_full));   // P^T(t+1) can start during dK(t), dP^T(t+1)
           }
           // dK += dS^T Q once dS^T is written
@@ -358,7 +362,7 @@ __global__ void __launch_bounds__(576, 1)
           if (more) {
             if (!(ok = wait_slot(io + 2))) break;
             tc_fence_after();
-            ss(128, sV, sRing + ((io + 2) % C::kStages) * C::kTile);
+            ss(128, sV, sRing + ((io + 2) % C::kStages) * C::kTile, C::kIdescSS);
             mma_commit_w(bar(ctl.dp_full));
           }
         }
@@ -376,6 +380,7 @@ __global__ void __launch_bounds__(576, 1)
     const int r = qd * 32 + lane;        // key row within the block
     const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
     const float cl = p.scale_log2;
+    const bool zero_scale = p.zero_scale != 0;
     uint32_t uit = 0, gblk = 0, item = 0;
     bool ok = true;
     for (uint32_t k = 0; ok; ++k, ++uit) {
@@ -424,11 +429,12 @@ __global__ void __launch_bounds__(576, 1)
           tmem_ld32(tmem + lane_off + 32 * h, sv);
           tmem_wait_ld();
           reg_fence(sv);
-          if (!full_vis) {
-            // Diagonal / window-edge block: 2^-inf = 0 for the invisible scores.
+          if (!full_vis || zero_scale) {
+            // Diagonal / window-edge block: 2^-inf = 0 for the invisible scores
+            // (scale = 0: every visible score is 0).
 #pragma unroll
             for (int col = 0; col < 32; ++col)
-              if (!bwd_visible(key, q0 + col, p)) sv[col] = 0xff800000u;
+              sv[col] = !bwd_visible(key, q0 + col, p) ? 0xff800000u : (zero_scale ? 0u : sv[col]);
           }
           const uint64_t c2 = f32x2_pack(cl, cl);
           uint32_t pk[16];
@@ -674,7 +680,9 @@ __global__ void __launch_bounds__(576, 1)
       auto slot_addr = [&](uint32_t it) { return sRing + (it % C::kStagesDQ) * C::kTile; };
       // [128 rows in TMEM at a_col] x [128 rows of the K-major tile b0]^T over K = D,
       // four k-steps per election.
-      auto ts_k = [&](uint32_t d_col, uint32_t a_col, uint32_t b0) {
+      // S = Q K^T negates K (its B operand) for a negative scale; dP does not.
+      const uint32_t idesc_s = C::kIdescSS | (p.neg_scale ? kIdescNegateB : 0u);
+      auto ts_k = [&](uint32_t d_col, uint32_t a_col, uint32_t b0, uint32_t idesc) {
         const uint64_t db = make_smem_desc(b0, 16, 1024, kSwizzle128B);
         const uint32_t ta = tmem + a_col;
 #pragma unroll
@@ -682,7 +690,7 @@ __global__ void __launch_bounds__(576, 1)
           const uint64_t o = g * 1024;
           mma_ts_x4_w<false>(tmem + d_col, ta + 32 * g, ta + 32 * g + 8, ta + 32 * g + 16,
                              ta + 32 * g + 24, db + o, db + o + 2, db + o + 4, db + o + 6,
-                             C::kIdescSS, g > 0 ? 1u : 0u);
+                             idesc, g > 0 ? 1u : 0u);
         }
       };
       // [128 x 128 bf16 in TMEM at a_col, keys [32h, 32h+32) at columns a_col +
@@ -710,9 +718,9 @@ __global__ void __launch_bounds__(576, 1)
         item += 2 * J;
         if (!(ok = wait_slot(base) && wait_slot(base + 1))) break;
         tc_fence_after();
-        ts_k(kColS, kColQ, slot_addr(base));
+        ts_k(kColS, kColQ, slot_addr(base), idesc_s);
         mma_commit_w(bar(ctl.s_full));
-        ts_k(kColDP, kColdO, slot_addr(base + 1));
+        ts_k(kColDP, kColdO, slot_addr(base + 1), C::kIdescSS);
         mma_commit_w(bar(ctl.dp_full));
         mma_commit_w(bar(ctl.empty[(base + 1) % C::kStagesDQ]));   // V_0 done
         for (int jj = 0; jj < J && ok; ++jj, ++gblk) {
@@ -722,7 +730,7 @@ __global__ void __launch_bounds__(576, 1)
           if (more) {
             if (!(ok = wait_w(bar(ctl.s_read), gblk & 1) && wait_slot(ik + 2))) break;
             tc_fence_after();
-            ts_k(kColS, kColQ, slot_addr(ik + 2));
+            ts_k(kColS, kColQ, slot_addr(ik + 2), idesc_s);
             mma_commit_w(bar(ctl.s_full));
           }
           // dQ += dS K_j once dS is written (over dP)
@@ -734,7 +742,7 @@ __global__ void __launch_bounds__(576, 1)
           if (more) {
             if (!(ok = wait_slot(ik + 3))) break;
             tc_fence_after();
-            ts_k(kColDP, kColdO, slot_addr(ik + 3));
+            ts_k(kColDP, kColdO, slot_addr(ik + 3), C::kIdescSS);
             mma_commit_w(bar(ctl.dp_full));
             mma_commit_w(bar(ctl.empty[(ik + 3) % C::kStagesDQ]));   // V_{jj+1} done
           }
@@ -752,6 +760,7 @@ __global__ void __launch_bounds__(576, 1)
     const int r = qd * 32 + lane;        // query row within the block
     const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
     const float cl = p.scale_log2;
+    const bool zero_scale = p.zero_scale != 0;
     uint32_t uit = 0, gblk = 0;
     bool ok = true;
     for (uint32_t k = 0; ok; ++k, ++uit) {
@@ -812,11 +821,12 @@ __global__ void __launch_bounds__(576, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(ctl.s_read));   // S(jj+1) may overwrite S now
-          if (!full_vis) {
-            // Diagonal / window-edge / ragged block: 2^-inf = 0 for invisible scores.
+          if (!full_vis || zero_scale) {
+            // Diagonal / window-edge / ragged block: 2^-inf = 0 for invisible scores
+            // (scale = 0: every visible score is 0).
 #pragma unroll
             for (int col = 0; col < 32; ++col)
-              if (!bwd_visible(k0 + col, q, p)) sv[col] = 0xff800000u;
+              sv[col] = !bwd_visible(k0 + col, q, p) ? 0xff800000u : (zero_scale ? 0u : sv[col]);
           }
           const uint64_t c2 = f32x2_pack(cl, cl);
           const uint64_t nl2 = f32x2_pack(-Lq, -Lq);

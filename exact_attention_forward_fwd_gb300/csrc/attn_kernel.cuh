@@ -31,7 +31,9 @@
 //   * TMEM columns: S/P tile 0 [0,128), S/P tile 1 [128,256), O tile 0
 //     [256,256+D), O tile 1 [256+D, 256+2D);
 //   * scale folded into exp2: p = 2^(s * scale*log2(e) - m), m kept in the
-//     same base-2 units;
+//     same base-2 units; a negative scale runs as s' = Q (-K)^T with |scale|
+//     (the MMA negates its B operand, exactly), so the multiplier the softmax
+//     sees is always positive; scale = 0 replaces every visible score by 0;
 //   * conditional rescaling: the reference max used for the exponentials is
 //     only moved (and O~, l rescaled) when the block's values against it grow
 //     too large.  Numerator and denominator always share the same reference,
@@ -58,8 +60,8 @@
 
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
-#include <mutex>
 
 #include "ptx.cuh"
 
@@ -83,7 +85,10 @@ struct AttnParams {
   int npairs;            // ceil(N / 256): query-tile pairs per head
   int num_units;         // BH * npairs
   int causal;
-  float scale_log2;      // scale * log2(e)
+  float scale_log2;      // |scale| * log2(e) (log2(e) when scale = 0)
+  int neg_scale;         // scale < 0: the score product negates its K operand, so the
+                         // softmax always sees a positive multiplier
+  int zero_scale;        // scale = 0: every visible score is 0 (uniform weights)
   unsigned long long timeout_ns;
   int skip_load;         // test hook: when > 0, the load warp stops after that many K/V loads
   // Split-KV mode (o_part != null): every (head, query-tile pair) is split into
@@ -409,6 +414,7 @@ __global__ void __launch_bounds__(384, 1)
       const uint64_t dQ = make_smem_desc(sQ, 16, 1024, kSwizzle128B);
       const uint64_t dK = make_smem_desc(sKV, 16, 1024, kSwizzle128B);
       const uint64_t dV = make_smem_desc(sKV, FP8 ? 16 : 16384, 1024, kSwizzle128B);
+      const uint32_t idesc_s = C::kIdescS | (p.neg_scale ? kIdescNegateB : 0u);
       auto s_mma = [&](int t, uint32_t kslot) {
         const uint64_t da = dQ + t * kTileUnits;
         const uint64_t db = dK + kslot * kTileUnits;
@@ -416,7 +422,7 @@ __global__ void __launch_bounds__(384, 1)
         for (int g = 0; g < C::kSKSteps / 4; ++g) {
           const uint64_t o = FP8 ? 0 : g * 1024;   // next 128-byte column slab (bf16, d = 128)
           mma_ss_x4_w<FP8>(tmem + 128 * t, da + o, da + o + 2, da + o + 4, da + o + 6, db + o,
-                           db + o + 2, db + o + 4, db + o + 6, C::kIdescS, g > 0 ? 1u : 0u);
+                           db + o + 2, db + o + 4, db + o + 6, idesc_s, g > 0 ? 1u : 0u);
         }
       };
       // O_t += P_t V over the keys of half `hf` of the block (P of each half is
@@ -520,6 +526,7 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t tS = tmem + lane_off + 128 * t;
     const uint32_t tO = tmem + lane_off + 256 + D * t;
     const float NEG_INF = __int_as_float(0xff800000);
+    const bool zero_scale = p.zero_scale != 0;
     uint32_t sit = 0, uit = 0;
     bool ok = true;
     // 64 columns of this thread's row of O_t from TMEM, times inv, as bf16 pairs.
@@ -598,9 +605,10 @@ __global__ void __launch_bounds__(384, 1)
           reg_fence(sr);
 #pragma unroll
           for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(sr[c]);
-          if (lim < 127 || lo > 0) {
+          if (lim < 127 || lo > 0 || zero_scale) {
 #pragma unroll
-            for (int c = 0; c < 128; ++c) x[c] = (c > lim || c < lo) ? NEG_INF : x[c];
+            for (int c = 0; c < 128; ++c)
+              x[c] = (c > lim || c < lo) ? NEG_INF : (zero_scale ? 0.0f : x[c]);
           }
         };
         auto row_max = [&](const float (&x)[128]) {
@@ -898,27 +906,18 @@ namespace gb300 {
 // Unit counters of the dynamic scheduler (one file-scope array per translation
 // unit).  Each launch takes the next of 64 counters in turn and zeroes it on
 // its stream first, so launches in flight on different streams do not share a
-// counter (unless 64 of them overlap).
+// counter (unless 64 of them overlap).  The array's device address is looked
+// up on every launch, for the device current then: a cached address would
+// outlive a context torn down and created again (cudaDeviceReset).
 static __device__ int g_unit_counter[64];
 
 static cudaError_t unit_counter(cudaStream_t stream, int** out) {
-  static std::mutex mu;
-  static int* base[64] = {};
-  static unsigned next = 0;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static std::atomic<unsigned> next{0};
+  void* a = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&a, g_unit_counter);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  int* c = nullptr;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    if (base[dev] == nullptr) {
-      void* a = nullptr;
-      if ((e = cudaGetSymbolAddress(&a, g_unit_counter)) != cudaSuccess) return e;
-      base[dev] = static_cast<int*>(a);
-    }
-    c = base[dev] + (next++ % 64);
-  }
+  if (a == nullptr) return cudaErrorInvalidSymbol;
+  int* c = static_cast<int*>(a) + (next.fetch_add(1u, std::memory_order_relaxed) % 64u);
   if ((e = cudaMemsetAsync(c, 0, sizeof(int), stream)) != cudaSuccess) return e;
   *out = c;
   return cudaSuccess;

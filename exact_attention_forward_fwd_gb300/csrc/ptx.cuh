@@ -259,6 +259,7 @@ __device__ __forceinline__ uint64_t make_smem_desc(uint32_t saddr, uint32_t lbo_
 
 // Instruction descriptor (32 bit) for kind::f16 / kind::f8f6f4, dense:
 //   [4,6) D format (1 = f32)   [7,10) A format   [10,13) B format
+//   [13] negate A              [14] negate B
 //   [15] A major (1 = MN)      [16] B major (1 = MN)
 //   [17,23) N >> 3             [24,29) M >> 4
 // Formats: kind::f16 -> 0 f16, 1 bf16; kind::f8f6f4 -> 0 e4m3, 1 e5m2.
@@ -268,6 +269,10 @@ __host__ __device__ constexpr uint32_t make_idesc(uint32_t M, uint32_t N, uint32
   return (1u << 4) | (a_fmt << 7) | (b_fmt << 10) | ((a_mn_major ? 1u : 0u) << 15) |
          ((b_mn_major ? 1u : 0u) << 16) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
+
+// Bit 14 of the instruction descriptor: negate the B operand (exact: a sign
+// flip of every element before the products).
+constexpr uint32_t kIdescNegateB = 1u << 14;
 
 // ---------------------------------------------------------------- MMA issue
 

@@ -26,12 +26,20 @@
  *     by attn_device_status().
  *   - Every bounded wait inside a kernel gives up after a time limit (1 s for
  *     the plain entry points), records ATTN_ERR_TIMEOUT, frees its tensor
- *     memory and returns; outputs are then unspecified.
- *   - The forward kernels hand out their work units dynamically from a counter
- *     in the library's own device memory (64 counters used in turn, each zeroed
- *     by a memset on the caller's stream before its launch; no allocation).
- *     The first call on a device looks the counters up (cudaGetSymbolAddress):
- *     make one call before capturing a stream into a CUDA graph.
+ *     memory and returns.  A kernel held up that long (a debugger, time
+ *     slicing with another context) therefore ends early: a call's outputs are
+ *     defined only while attn_device_status() reports ATTN_OK.  A caller that
+ *     cannot rule such delays out checks it after its results are complete.
+ *   - The kernels hand out their work units dynamically from counters in the
+ *     library's own device memory (64 counters used in turn, each zeroed by a
+ *     memset on the caller's stream before its launch; no allocation).  Every
+ *     call looks their device address up (cudaGetSymbolAddress) for the
+ *     current device; the first call on a device loads the library's device
+ *     code there: make one call before capturing a stream into a CUDA graph.
+ *   - scale may be any finite value.  A negative scale is computed as
+ *     |scale| * (q . (-k)): the score product negates its K operand, which is
+ *     exact.  scale = 0 gives every visible key the same weight (O = mean of
+ *     the visible V rows, lse = log of their count).
  */
 #ifndef GB300_ATTN_H
 #define GB300_ATTN_H
@@ -66,7 +74,8 @@ enum attn_dtype { ATTN_BF16 = 0 };
  *   o       : bf16 [B, H, N, d], written (round to nearest even).
  *   lse     : f32 [B, H, N] logsumexp of the scaled scores, written; may be NULL.
  *   B, H, N : >= 1 (B * H < 2^31, N < 2^31).   d : 64 or 128.
- *   scale   : finite multiplier of q.k (usually 1/sqrt(d)).
+ *   scale   : finite multiplier of q.k (usually 1/sqrt(d)); negative and zero
+ *             values are computed exactly as the definition says.
  *   causal  : 0 or 1.   dtype : ATTN_BF16.
  * Errors: ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED (d, dtype, a device other than sm_103),
  * ATTN_ERR_ALIGNMENT (any of q, k, v, o not 16-byte aligned, lse not 4-byte aligned),
@@ -133,9 +142,10 @@ ATTN_API int attn_fwd_splitkv(const void* q, const void* k, const void* v, void*
  *   is written earlier in the same call.
  *   Calls share the one array: two calls that overlap in time (different
  *   streams or host threads without ordering) race and give undefined
- *   results; order them.  The first call on each device looks the array's
- *   address up (cudaGetSymbolAddress with that device current, ATTN_ERR_CUDA
- *   if that fails); that first call should come before any stream capture.
+ *   results; order them.  Every call looks the array's device address up
+ *   (cudaGetSymbolAddress with the calling device current, ATTN_ERR_CUDA if
+ *   that fails); the first call on a device also loads the library's device
+ *   code there, so that first call should come before any stream capture.
  *   The call makes no cudaMalloc, cudaFree or other allocating call. */
 ATTN_API int attn_fwd_splitkv_static(const void* q, const void* k, const void* v, void* o,
                                      float* lse, int B, int H, int H_kv, int N, int d,
@@ -185,7 +195,13 @@ ATTN_API int attn_fp8_prep(const void* x, void* x8, float* block_scale, const si
                   int H, int N, int d, int transpose_out, attn_stream_t stream);
 
 /* Exact attention forward with E4M3 operands (f32 accumulation, f32 softmax
- * statistics, bf16 output).  Score tile j of query block i is
+ * statistics, bf16 output): the FP8 forward of "FlashAttention-3: How Warp
+ * Specialization, Asynchronous TMA Tiling, and FP8 Hardware Acceleration Scale
+ * Attention on Hopper GPUs", section 4 (block-wise scaling: one scale per
+ * block of each operand, so a score tile is s_Q * s_K * (Q8 K8^T)), with the
+ * split of "4.3 FlashAttention 2 & 3", section "What stays in higher
+ * precision" (operands and P in FP8; accumulators, the running max and the
+ * row sums in f32).  Score tile j of query block i is
  * q_scale[i] * k_scale[j] * (Q8_i K8_j^T) * scale.  P is quantised to E4M3
  * with V's block scale folded in (p * 1.75 * v_scale[j] / max_j v_scale[j],
  * p <= 2^8 against the running reference maximum, so P' <= 448).

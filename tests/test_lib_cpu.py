@@ -76,6 +76,16 @@ def test_validation_codes(L):
                             None) == ga.ATTN_ERR_INVALID_ARG
 
 
+def test_every_finite_scale_is_accepted(L):
+    """Negative and zero scales are valid (the header defines them); only
+    non-finite ones are refused.  A misaligned O makes every call stop at the
+    alignment check, which comes after the scale check, so nothing launches."""
+    for scale in (-1.0, -0.125, 0.0, -0.0, 1e-30, 3.0):
+        assert _fwd(L, o=M, scale=scale) == ga.ATTN_ERR_ALIGNMENT, scale
+    for scale in (float("nan"), float("inf"), float("-inf")):
+        assert _fwd(L, o=M, scale=scale) == ga.ATTN_ERR_INVALID_ARG, scale
+
+
 def test_ex_validation_codes(L):
     ex = lambda H=4, H_kv=2, causal=1, window=0, d=128: L.attn_fwd_ex(
         A, A, A, A, None, 1, H, H_kv, 256, d, 0.1, causal, window, 0, None)

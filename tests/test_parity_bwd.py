@@ -145,3 +145,15 @@ def test_errors():
                            64, 0.125, 0, 0, q.data_ptr(), need, None)
     assert rc == ga.ATTN_ERR_INVALID_ARG   # lse is required
     assert ga.device_status() == 0
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("scale", [-1.0, -0.125, 0.0])
+def test_negative_and_zero_scale(scale, d, causal):
+    """The score products negate K (Q in the key-major kernel) for a negative
+    scale, and dQ, dK carry the signed scale; scale = 0 gives uniform P, and
+    dQ = dK = 0."""
+    q, k, v = inputs.make_qkv(1, 2, 300, d, seed=900 + d + int(causal))
+    dO = _make_dO(1, 2, 300, d, seed=901)
+    _full(q, k, v, dO, causal, scale=scale)
