@@ -104,9 +104,13 @@ __global__ void __launch_bounds__(256) fp8_prep_kernel(const uint16_t* __restric
   // the correctly rounded reciprocal, then one correction q + RN(x - q s) r
   // (the residual is exact by FMA) -- Markstein's final step, which yields the
   // correctly rounded binary32 quotient when r = RN(1 / s).  The sign is taken
-  // from q so that x = -0 gives -0 (the correction would add +0).
-  const float rcp = __frcp_rn(s);
+  // from q so that x = -0 gives -0 (the correction would add +0).  A block
+  // whose scale is subnormal (amax below 448 * 2^-126) divides instead: 1 / s
+  // may then exceed the f32 range.  The branch is uniform over the block.
+  const bool tiny = s < 1.17549435e-38f;   // 2^-126, the smallest normal f32
+  const float rcp = tiny ? 0.0f : __frcp_rn(s);
   auto div_s = [&](float xv) {
+    if (tiny) return __fdiv_rn(xv, s);
     const float q = xv * rcp;
     const float res = fmaf(-q, s, xv);
     return copysignf(fmaf(res, rcp, q), q);
