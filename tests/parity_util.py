@@ -3,13 +3,17 @@ import numpy as np
 import torch
 
 # Acceptance on bf16 outputs against the float64 oracle (element by element).
-# |O - O_ref| <= 1e-2 + 2^-9 |O_ref|: the 1e-2 bound on top of the half-unit
-# rounding of the bf16 output format itself (a bf16 O in [4, 8) cannot be
-# nearer than 2^-6 to a value between two representable numbers; on the K*8
-# workload the exactly rounded oracle result is already 0.015 away).  The mean
-# abs bound gets the same allowance on average, 1e-3 + 2^-9 mean|O_ref|: for
-# rows that see one or two keys (short windows) O is of unit size and rounding
-# it to bf16 alone averages about 1e-3; for long rows the term is ~4e-5.
+# Max abs: |O - O_ref| <= 1e-2 + 2^-9 |O_ref|, the 1e-2 bound on top of the
+# rounding of the bf16 output format itself (a bf16 O in [4, 8) has spacing
+# 2^-5; on the K*8 workload the exactly rounded oracle result is already 0.0155
+# away, so the literal 1e-2 cannot be met by any bf16 output).
+# Mean abs: 1e-3 as stated, with one exception that a test must ask for: where
+# rounding the exact result to bf16 alone already costs a sizeable part of the
+# bound, the gate is 1e-3 beyond that floor, mean |bf16(O_ref) - O_ref|, which
+# is computed from the oracle's own result.  That is the case for outputs of
+# unit size: rows that see one or a few keys, or one dominant key.  The five
+# workloads are gated as written (their floors: 8.1e-4 on the 2048-token K*8
+# workload, 2e-5 to 1.1e-4 on the others).
 BF16_MAX_ABS = 1e-2
 BF16_OUT_HALF_ULP = 2.0 ** -9
 BF16_MEAN_ABS = 1e-3
@@ -29,12 +33,19 @@ def f64(t: torch.Tensor) -> np.ndarray:
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
+def bf16_round(x: np.ndarray) -> np.ndarray:
+    """x rounded to bfloat16 (nearest even), back in float64."""
+    return torch.from_numpy(np.ascontiguousarray(x)).to(torch.bfloat16).double().numpy()
+
+
 def metrics(o_gpu, lse_gpu, O_ref, L_ref):
     o = f64(o_gpu) if isinstance(o_gpu, torch.Tensor) else o_gpu
     lse = f64(lse_gpu) if isinstance(lse_gpu, torch.Tensor) else lse_gpu
     err = np.abs(o - O_ref)
-    lerr = np.abs(lse - L_ref)
+    fin = np.isfinite(L_ref)
+    lerr = np.where(fin, np.abs(lse - L_ref), np.where(lse == L_ref, 0.0, np.inf))
     return {
+        "floor_mean": float(np.abs(bf16_round(O_ref) - O_ref).mean()),
         "max_abs": float(err.max()),
         "max_excess": float((err - BF16_OUT_HALF_ULP * np.abs(O_ref)).max()),
         "mean_abs": float(err.mean()),
@@ -42,16 +53,19 @@ def metrics(o_gpu, lse_gpu, O_ref, L_ref):
         "rmse": float(np.sqrt((err ** 2).mean())),
         "rel_rmse": float(np.sqrt((err ** 2).mean() / max((O_ref ** 2).mean(), 1e-300))),
         "lse_max_abs": float(lerr.max()),
-        "finite": bool(np.isfinite(o).all() and np.isfinite(lse).all()),
+        "finite": bool(np.isfinite(o).all() and np.isfinite(lse[fin]).all()),
     }
 
 
-def assert_bf16_parity(m, what=""):
+def assert_bf16_parity(m, what="", rounding_floor=False):
+    """The bf16 gates.  rounding_floor: the mean abs gate is taken beyond the
+    output-rounding floor (unit-size outputs and the K*8 workload only)."""
     assert m["finite"], f"{what}: non-finite output"
     assert m["max_excess"] <= BF16_MAX_ABS, \
         f"{what}: max abs {m['max_abs']:.3e} (beyond output rounding {m['max_excess']:.3e})"
-    assert m["mean_abs"] <= BF16_MEAN_ABS + m["mean_half_ulp"], \
-        f"{what}: mean abs {m['mean_abs']:.3e} (output rounding allowance {m['mean_half_ulp']:.1e})"
+    floor = m["floor_mean"] if rounding_floor else 0.0
+    assert m["mean_abs"] <= BF16_MEAN_ABS + floor, \
+        f"{what}: mean abs {m['mean_abs']:.3e} (gate 1e-3 + floor {floor:.1e})"
     assert m["lse_max_abs"] <= LSE_MAX_ABS, f"{what}: lse max abs {m['lse_max_abs']:.3e}"
 
 

@@ -48,4 +48,4 @@ def test_missing_tiles_time_out_and_context_survives(skip):
     qs, ks, vs = inputs.make_qkv(1, 2, 300, 64, seed=23)
     o, lse = ga.attn_fwd(qs.cuda(), ks.cuda(), vs.cuda(), causal=True)
     O, L = oa.attention(f64(qs), f64(ks), f64(vs), 64 ** -0.5, True)
-    assert_bf16_parity(metrics(o.cpu(), lse.cpu(), O, L), "after timeout")
+    assert_bf16_parity(metrics(o.cpu(), lse.cpu(), O, L), "after timeout", rounding_floor=True)

@@ -42,20 +42,23 @@ def _run(q, k, v, causal, scale=None, rows=None):
 @pytest.mark.parametrize("N", [1, 7, 128, 129, 255, 256, 257, 300, 640, 1000])
 def test_small_shapes(N, d, causal):
     q, k, v = inputs.make_qkv(2, 3, N, d, seed=N * 7 + d + int(causal))
-    assert_bf16_parity(_run(q, k, v, causal), f"N={N} d={d} causal={causal}")
+    # Short rows (N <= 7, and the first rows of every causal case) give O of
+    # unit size: the gate is taken beyond its bf16 rounding.
+    assert_bf16_parity(_run(q, k, v, causal), f"N={N} d={d} causal={causal}", rounding_floor=True)
 
 
 @pytest.mark.parametrize("causal", [False, True])
 def test_more_units_than_sms(causal):
     """B*H*pairs = 512 units: every CTA of the persistent grid runs several."""
     q, k, v = inputs.make_qkv(16, 16, 300, 64, seed=77)
-    assert_bf16_parity(_run(q, k, v, causal), "16x16x300")
+    assert_bf16_parity(_run(q, k, v, causal), "16x16x300", rounding_floor=causal)
 
 
 @pytest.mark.parametrize("scale", [1.0, 0.01, 0.3])
 def test_other_scales(scale):
     q, k, v = inputs.make_qkv(1, 2, 384, 128, seed=5)
-    assert_bf16_parity(_run(q, k, v, True, scale=scale), f"scale={scale}")
+    # scale 1: scores of spread ~11, rows nearly one-hot, O of unit size.
+    assert_bf16_parity(_run(q, k, v, True, scale=scale), f"scale={scale}", rounding_floor=True)
 
 
 @pytest.mark.parametrize("name", ["n256_d64", "n2048_d128", "n2048_d128_causal", "n2048_d128_k8",
@@ -65,6 +68,9 @@ def test_workload_all_rows(name):
     q, k, v = inputs.workload_inputs(w)
     m = _run(q, k, v, w.causal, w.scale)
     print(name, m)
+    # The stated mean abs gate as written on every workload, the K*8 ones
+    # included (measured 9.0e-4 there, of which bf16 rounding of the exact
+    # result alone is 8.1e-4).
     assert_bf16_parity(m, name)
 
 
@@ -134,18 +140,19 @@ def _run_ex(q, k, v, causal, window, rows=None):
 @pytest.mark.parametrize("causal", [False, True])
 def test_grouped_query_heads(H_kv, d, causal):
     q, k, v = inputs.make_qkv(2, 8, 700, d, seed=300 + H_kv + d, H_kv=H_kv)
-    assert_bf16_parity(_run_ex(q, k, v, causal, 0), f"H_kv={H_kv} d={d}")
+    assert_bf16_parity(_run_ex(q, k, v, causal, 0), f"H_kv={H_kv} d={d}", rounding_floor=causal)
 
 
 @pytest.mark.parametrize("window", [1, 2, 64, 127, 128, 129, 255, 256, 300, 5000])
 def test_sliding_window(window):
     q, k, v = inputs.make_qkv(1, 4, 1000, 128, seed=400 + window, H_kv=2)
-    assert_bf16_parity(_run_ex(q, k, v, True, window), f"window={window}")
+    # Rows that see 1 or 2 keys have O of unit size.
+    assert_bf16_parity(_run_ex(q, k, v, True, window), f"window={window}", rounding_floor=True)
 
 
 def test_sliding_window_d64_ragged():
     q, k, v = inputs.make_qkv(3, 2, 777, 64, seed=501)
-    assert_bf16_parity(_run_ex(q, k, v, True, 200), "window=200 d=64")
+    assert_bf16_parity(_run_ex(q, k, v, True, 200), "window=200 d=64", rounding_floor=True)
 
 
 def test_gqa_window_workload_sampled_rows():

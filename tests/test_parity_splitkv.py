@@ -38,7 +38,9 @@ def _run(q, k, v, causal, splits, window=0, rows=None, scale=None):
 @pytest.mark.parametrize("N,splits", [(129, 2), (300, 3), (640, 2), (640, 5), (1000, 7)])
 def test_small_shapes(N, splits, d, causal):
     q, k, v = inputs.make_qkv(1, 3, N, d, seed=N * 11 + d + splits + int(causal))
-    assert_bf16_parity(_run(q, k, v, causal, splits), f"N={N} S={splits} d={d} causal={causal}")
+    # Causal rows near the start see a few keys: O of unit size (gate beyond its rounding).
+    assert_bf16_parity(_run(q, k, v, causal, splits), f"N={N} S={splits} d={d} causal={causal}",
+                       rounding_floor=causal)
 
 
 @pytest.mark.parametrize("causal", [False, True])
@@ -46,7 +48,8 @@ def test_small_shapes(N, splits, d, causal):
 def test_more_splits_than_key_blocks(splits, causal):
     """N = 200 has two 128-key blocks: most ranges are empty and get weight 0."""
     q, k, v = inputs.make_qkv(2, 2, 200, 128, seed=splits + 100 * int(causal))
-    assert_bf16_parity(_run(q, k, v, causal, splits), f"S={splits} causal={causal}")
+    assert_bf16_parity(_run(q, k, v, causal, splits), f"S={splits} causal={causal}",
+                       rounding_floor=causal)
 
 
 @pytest.mark.parametrize("d", [64, 128])
@@ -73,7 +76,8 @@ def test_grouped_heads_and_window(H_kv, window, splits):
                                  num_splits=splits)
     assert ga.device_status() == 0
     O_ref, L_ref = oa.attention(f64(q), f64(k_full), f64(v_full), 128 ** -0.5, True, window=window)
-    assert_bf16_parity(metrics(o.cpu(), lse.cpu(), O_ref, L_ref), f"H_kv={H_kv} w={window}")
+    assert_bf16_parity(metrics(o.cpu(), lse.cpu(), O_ref, L_ref), f"H_kv={H_kv} w={window}",
+                       rounding_floor=True)
 
 
 @pytest.mark.parametrize("name", ["n8192_d128_b1h2", "n8192_d128_b1h2_causal"])
