@@ -32,7 +32,7 @@ def _worker(rank, ws, port, out):
 
 def test_replicas_aggregate_over_two_gloo_ranks():
     ws = 2
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.spawn(_worker, args=(ws, _free_port(), out), nprocs=ws, join=True)
         res = dict(out)
