@@ -41,6 +41,24 @@ def test_two_calls_in_a_row_match_workspace_entry(B, H, N, d, causal, splits):
         assert torch.equal(l, ref_l)
 
 
+def test_fewer_splits_after_more_ignores_stale_partials():
+    """A call with many key ranges leaves partial results all over the shared
+    array; a following call with fewer ranges, several of them empty (causal
+    pairs near the start have fewer key blocks than ranges), must read only
+    what it wrote itself: bit for bit what attn_fwd_splitkv gives with a fresh
+    workspace."""
+    # 16 ranges x 4096 rows x 129 floats = 34 MB of the 64 MiB array.
+    q, k, v = [t.cuda() for t in inputs.make_qkv(1, 1, 4096, 128, seed=41)]
+    ga.attn_fwd_splitkv_static(q, k, v, causal=True, num_splits=16)
+    for splits in (5, 3):
+        ref_o, ref_l = ga.attn_fwd_splitkv(q, k, v, causal=True, num_splits=splits)
+        o, l = ga.attn_fwd_splitkv_static(q, k, v, causal=True, num_splits=splits)
+        torch.cuda.synchronize()
+        assert ga.device_status() == 0
+        assert torch.equal(o, ref_o)
+        assert torch.equal(l, ref_l)
+
+
 def test_call_allocates_no_device_memory():
     q, k, v = [t.cuda() for t in inputs.make_qkv(1, 2, 2048, 128, seed=9)]
     o = torch.empty_like(q)
@@ -53,8 +71,11 @@ def test_call_allocates_no_device_memory():
         ga.attn_fwd_splitkv_static(q, k, v, num_splits=4, out=o, lse=lse)
     torch.cuda.synchronize()
     free1, _ = torch.cuda.mem_get_info()
-    assert free1 == free0
+    # torch's own count is exact; the device-wide free memory can also move
+    # with other users of the GPU, so it only bounds an allocation of the
+    # scratch's size (64 MiB) from below.
     assert torch.cuda.memory_allocated() == alloc0
+    assert free1 >= free0 - (8 << 20)
 
 
 def test_oversize_request_is_refused():
