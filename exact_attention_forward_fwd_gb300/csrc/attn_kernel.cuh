@@ -39,11 +39,14 @@
 //     too large.  Numerator and denominator always share the same reference,
 //     so the result stays exact.  The exponentials are taken against the
 //     current reference and the block's sum of p decides: a sum of at most
-//     2^8 bounds every p by 2^8 and the pass stands; otherwise (rare after a
-//     unit's first block) the reference moves to the block's max and the
-//     block, still in TMEM, is taken again.  No exponential waits for a row
+//     2^32 bounds every p by 2^32 and the pass stands (f32 O~ and l then stay
+//     below 2^56 times max|V| for any sequence length); otherwise (rare after
+//     a unit's first block, even on rows as sharp as scores with a spread of
+//     10 in base 2) the reference moves to the block's max and the block,
+//     still in registers, is taken again.  No exponential waits for a row
 //     max.  The FP8 path takes the block's max first instead and moves the
-//     reference only when that max exceeds it by more than 8, so p <= 2^8.
+//     reference only when that max exceeds it by more than 8, so p <= 2^8
+//     (P must fit E4M3, whose largest value is 448).
 //   * because every tcgen05.commit tracks all earlier MMAs of the issuing
 //     thread, the arrival of S_t(j) also proves O_t += P_t(j-1) V(j-1) is
 //     complete: a rescale of O~ right after waiting for S_t(j) is race-free.
@@ -122,13 +125,18 @@ struct KCfg {
   static constexpr uint32_t kRegsOther = 56;
   static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsOther <= kThreads * kLaunchRegs,
                 "register split exceeds the block's pool");
-  static constexpr float kSumLimit = 256.0f;              // 2^8: bound on a block's sum of p
+  static constexpr float kSumLimit = 4294967296.0f;       // bf16: 2^32, bound on a block's sum of p
   static constexpr float kTauLog2 = 8.0f;                 // FP8: move the reference when a block max exceeds it by more
   static constexpr float kPScale = 1.75f;                 // FP8: P' = p * kPScale * s_V(j) / max s_V <= 256 * 1.75 = 448
   // Causal: tile 0 skips a pair's last key block (wholly above its rows).  bf16
   // at d = 128 only: the FP8 and d = 64 kernels measured 2 % slower with the
   // extra branches in their issue loop than the work saved.
   static constexpr bool kSkipDiag = !FP8 && D == 128;
+  // FP8: P (one byte per key, 128 bytes per row) goes to shared memory -- the
+  // region that stages O in the epilogue -- instead of over S in tensor
+  // memory, so a tile's next S product can start as soon as its softmax has
+  // read S, and P.V reads P as an SS operand.
+  static constexpr bool kPSmem = FP8;
   static constexpr int kSKSteps = FP8 ? D / 32 : D / 16;  // k-steps of S = Q K^T
   static constexpr int kPVSteps = FP8 ? 4 : 8;            // k-steps of O += P V (128 keys)
   static constexpr uint32_t kIdescS =
@@ -144,6 +152,8 @@ struct SmemCtl {
   uint64_t q_empty[2];
   uint64_t s_full[2];
   uint64_t p_ready[2][2];   // [tile][half of the block's keys] (bf16 signals all keys on [t][0])
+  uint64_t s_free[2];       // FP8: the tile's S has been read (its TMEM columns may be overwritten)
+  uint64_t p_free[2];       // FP8: the tile's P.V is done (its P buffer may be overwritten)
   uint64_t o_final[2];
   uint64_t drain;
   uint64_t unit_full[4];    // ring of work-unit indices handed out by the load warp
@@ -253,6 +263,7 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t sQ = smem_addr(smem);                         // Q tile 0, Q tile 1
   const uint32_t sKV = sQ + 2 * C::kTileBytes;                 // ring of K / V tiles
   const uint32_t sO = sKV + C::kStages * C::kTileBytes;        // O staging (d = 128), 4 KB per softmax warp
+                                                               // (FP8: also P, 128 bytes per row)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
@@ -272,6 +283,8 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(bar(ctl.p_ready[t][0]), FP8 ? 4 : 128);
       mbar_init(bar(ctl.p_ready[t][1]), FP8 ? 4 : 128);
       mbar_init(bar(ctl.o_final[t]), 1);
+      mbar_init(bar(ctl.s_free[t]), 4);
+      mbar_init(bar(ctl.p_free[t]), 1);
     }
     mbar_init(bar(ctl.drain), 1);
     for (int s = 0; s < 4; ++s) {
@@ -446,6 +459,75 @@ __global__ void __launch_bounds__(384, 1)
       auto wait_item = [&](uint32_t it) {
         return wait_w(ctl.kv_full[it % C::kStages], (it / C::kStages) & 1);
       };
+      if constexpr (C::kPSmem) {
+        // FP8, P in shared memory.  S_t(j+1) is issued once the softmax has
+        // read S_t(j) (s_free) and K_{j+1} has landed; P_t(j).V_j once both
+        // halves of P_t(j) are in shared memory.  A tile's softmax therefore
+        // never waits for its own products: the next S is computed while it
+        // works on the current block.  p_free (a commit after each P.V) tells
+        // the softmax that the P buffer may be refilled and O rescaled.
+        uint32_t ns[2] = {0, 0};   // S products issued per tile
+        uint32_t npv = 0;          // P.V products issued per tile
+        const uint64_t dP = make_smem_desc(sO, 16, 1024, kSwizzle128B);
+        auto issue_s = [&](int t, uint32_t kslot) -> bool {
+          if (ns[t] > 0 && !wait_w(ctl.s_free[t], (ns[t] - 1) & 1)) return false;
+          ++ns[t];
+          tc_fence_after();
+          s_mma(t, kslot);
+          mma_commit_w(bar(ctl.s_full[t]));
+          return true;
+        };
+        // O_t (+)= P_t V over the block's 128 keys (four K = 32 steps) once
+        // P_t is in shared memory.
+        auto issue_pv = [&](int t, uint32_t vslot, bool acc) -> bool {
+          const uint64_t da = dP + t * (uint64_t)(C::kOStageBytes >> 4);
+          const uint64_t db = dV + vslot * kTileUnits;
+          if (!wait_w(ctl.p_ready[t][0], npv & 1)) return false;
+          tc_fence_after();
+          mma_ss_x4_w<true>(tmem + 256 + D * t, da, da + 2, da + 4, da + 6, db, db + 2, db + 4,
+                            db + 6, C::kIdescPV, acc ? 1u : 0u);
+          mma_commit_w(bar(ctl.p_free[t]));
+          return true;
+        };
+        for (uint32_t k = 0; ok; ++k) {
+          const int u = take_unit(k, ok);
+          if (u < 0) break;
+          const Unit w = unit_of(u, p);
+          const int J = w.nblocks;
+          if (J == 0) continue;
+          ok = wait_w(ctl.q_full[0], uit & 1) && wait_w(ctl.q_full[1], uit & 1);
+          if (!ok) break;
+          const uint32_t base = item;   // K_j = base + 2j, V_j = base + 2j + 1
+          item += 2 * J;
+          if (!(ok = wait_item(base))) break;
+          if (!(ok = issue_s(0, base % C::kStages) && issue_s(1, base % C::kStages))) break;
+          mma_commit_w(bar(ctl.kv_empty[base % C::kStages]));
+          if (J == 1) {
+            mma_commit_w(bar(ctl.q_empty[0]));
+            mma_commit_w(bar(ctl.q_empty[1]));
+          }
+          for (int j = 0; j < J && ok; ++j) {
+            const uint32_t iv = base + 2 * j + 1, ik = base + 2 * j + 2;
+            if (j + 1 < J) {
+              if (!(ok = wait_item(ik))) break;
+              if (!(ok = issue_s(0, ik % C::kStages) && issue_s(1, ik % C::kStages))) break;
+              mma_commit_w(bar(ctl.kv_empty[ik % C::kStages]));
+              if (j + 2 == J) {
+                mma_commit_w(bar(ctl.q_empty[0]));
+                mma_commit_w(bar(ctl.q_empty[1]));
+              }
+            }
+            if (!(ok = wait_item(iv))) break;
+            if (!(ok = issue_pv(0, iv % C::kStages, j > 0))) break;
+            if (j == J - 1) mma_commit_w(bar(ctl.o_final[0]));
+            if (!(ok = issue_pv(1, iv % C::kStages, j > 0))) break;
+            mma_commit_w(bar(ctl.kv_empty[iv % C::kStages]));
+            if (j == J - 1) mma_commit_w(bar(ctl.o_final[1]));
+            ++npv;
+          }
+          ++uit;
+        }
+      } else
       for (uint32_t k = 0; ok; ++k) {
         const int u = take_unit(k, ok);
         if (u < 0) break;
@@ -528,6 +610,7 @@ __global__ void __launch_bounds__(384, 1)
     const float NEG_INF = __int_as_float(0xff800000);
     const bool zero_scale = p.zero_scale != 0;
     uint32_t sit = 0, uit = 0;
+    uint32_t np = 0;   // FP8: P blocks this tile has written (phase of p_free)
     bool ok = true;
     // 64 columns of this thread's row of O_t from TMEM, times inv, as bf16 pairs.
     auto load_o_bf16 = [&](int col, float inv_o, uint32_t (&pk)[32]) {
@@ -569,29 +652,44 @@ __global__ void __launch_bounds__(384, 1)
       const int lo_row = p.window > 0 ? row - p.window + 1 : 0;      // first visible key
       float m_ref = NEG_INF, ell = 0.0f;   // reference max (base 2), sum of f32 p
       float ell_r = 0.0f;                   // sum of p as rounded into P (bf16 path)
-      float q_s = 1.0f, v_smax = 1.0f;
+      float q_s = 1.0f, v_smax = 1.0f, inv_vmax = 1.0f;
+      float ks_nx = 1.0f, vs_nx = 1.0f;   // FP8: K and V scales of the next block, loaded a block ahead
+      const float* ksc = FP8 ? p.k_scale + (size_t)w.bhk * p.nkb : nullptr;
+      const float* vsc = FP8 ? p.v_scale + (size_t)w.bhk * p.nkb : nullptr;
       if (FP8) {
         const int qb = w.pair * 2 + t;
         q_s = (qb < p.nkb) ? __ldg(p.q_scale + (size_t)w.bh * p.nkb + qb) : 1.0f;
         float mx = 0.0f;
-        for (int b = lane; b < p.nkb; b += 32) mx = fmaxf(mx, __ldg(p.v_scale + (size_t)w.bhk * p.nkb + b));
+        for (int b = lane; b < p.nkb; b += 32) mx = fmaxf(mx, __ldg(vsc + b));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         v_smax = mx;
+        inv_vmax = C::kPScale / v_smax;
+        ks_nx = __ldg(ksc + w.j0);
+        vs_nx = __ldg(vsc + w.j0);
       }
       const int nb_t = w.nblocks - ((C::kSkipDiag && t == 0 && w.skip0) ? 1 : 0);   // tile 0 may skip the last
       for (int jj = 0; jj < nb_t; ++jj) {
         const int j = w.j0 + jj;   // key block
-        ok = wait_bounded(bar(ctl.s_full[t]), sit++ & 1, wc);
+        // FP8: the block's score factor and P fold (V's block scale over the
+        // head's largest, times 1.75), from scales loaded one block ahead.
+        float cj = p.scale_log2;
+        float v_fold = 1.0f, inv_vfold = 1.0f, lg_vfold = 0.0f;
+        if (FP8) {
+          cj *= q_s * ks_nx;
+          v_fold = vs_nx * inv_vmax;
+          if (jj + 1 < nb_t) {
+            ks_nx = __ldg(ksc + j + 1);
+            vs_nx = __ldg(vsc + j + 1);
+          }
+          inv_vfold = __frcp_rn(v_fold);
+          lg_vfold = __log2f(v_fold);
+        }
+        ok = mbar_test_wait(bar(ctl.s_full[t]), sit & 1) || wait_bounded(bar(ctl.s_full[t]), sit & 1, wc);
+        ++sit;
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
-        float cj = p.scale_log2;
-        float v_fold = 1.0f;
-        if (FP8) {
-          cj *= q_s * __ldg(p.k_scale + (size_t)w.bhk * p.nkb + j);
-          v_fold = C::kPScale * __ldg(p.v_scale + (size_t)w.bhk * p.nkb + j) / v_smax;
-        }
         const int lim = lim_row - j * 128;    // columns > lim are invisible
         const int lo = lo_row - j * 128;      // columns < lo are invisible (window)
         // S of this block -> x (raw scores; invisible columns -inf).
@@ -648,7 +746,7 @@ __global__ void __launch_bounds__(384, 1)
           // returns their sum of p.
           auto exps_half = [&](const float (&x)[128], int hf) -> float {
             const float m_use = (m_ref == NEG_INF) ? 0.0f : m_ref;
-            const float m_f = m_use - __log2f(v_fold);
+            const float m_f = m_use - lg_vfold;
             const uint64_t c2 = f32x2_pack(cj, cj);
             const uint64_t nm2 = f32x2_pack(-m_f, -m_f);
             uint64_t s01 = 0, s23 = 0;   // (0.f, 0.f)
@@ -667,7 +765,7 @@ __global__ void __launch_bounds__(384, 1)
             }
             float a0, a1;
             f32x2_unpack(f32x2_add(s01, s23), a0, a1);
-            return (a0 + a1) / v_fold;
+            return (a0 + a1) * inv_vfold;
           };
           {
             // The block's max first: E4M3 P must never saturate, and with the
@@ -675,37 +773,74 @@ __global__ void __launch_bounds__(384, 1)
             // enough that retaking a block would cost more than this pass.
             float x[128];
             load_s(x);
+            // S is in registers now: the tile's next S product may overwrite it.
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(ctl.s_free[t]));
             const float m_blk = row_max(x) * cj;
             const bool need = m_blk > m_ref + C::kTauLog2;
             const float m_new = need ? m_blk : m_ref;
             const float alpha = need ? ex2_approx(m_ref - m_new) : 1.0f;   // 0 when m_ref = -inf
-            if (jj > 0 && __any_sync(0xffffffffu, need)) rescale_o(alpha);
+            // The previous block's P.V must be done before O_t is rescaled or
+            // the P buffer refilled (it was issued as that block's P landed).
+            bool pfree = np == 0;
+            auto wait_pfree = [&]() {
+              if (pfree) return true;
+              pfree = true;
+              const uint32_t pb = bar(ctl.p_free[t]), ph = (np - 1) & 1;
+              const bool w_ok =
+                  __all_sync(0xffffffffu, mbar_test_wait(pb, ph) || wait_bounded(pb, ph, wc));
+              tc_fence_after();
+              return w_ok;
+            };
+            if (jj > 0 && __any_sync(0xffffffffu, need)) {
+              if (!(ok = wait_pfree())) break;
+              rescale_o(alpha);
+              tmem_wait_st();   // the rescaled O is in TMEM before P.V (signalled below) adds to it
+              tc_fence_before();
+            }
             ell *= alpha;
             m_ref = m_new;
-            // keys [64hf, 64hf+64) -> P columns [16hf, 16hf+16), each half
-            // signalled as soon as it is stored, so the first half's P.V runs
-            // during the second half's exponentials.
+            // keys [64hf, 64hf+64) -> bytes [64hf, 64hf+64) of this row of the
+            // tile's P buffer (the 128-byte swizzle of a K-major operand: 16-byte
+            // chunk c of row r at position c ^ (r & 7)); the first half is stored
+            // while the second half's exponentials run, and P.V is signalled once
+            // (it is off the softmax's path: the next S is already computed).
+            const uint32_t prow = sO + t * C::kOStageBytes + r * 128;
             e_sum = 0.0f;
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
               e_sum += exps_half(x, hf);
-              __syncwarp();   // tcgen05.st is warp-collective
-              tmem_st16(tS + 16 * hf, *reinterpret_cast<uint32_t(*)[16]>(&pk[16 * hf]));
-              tmem_wait_st();
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(bar(ctl.p_ready[t][hf]));
+              if (hf == 0) {
+                if (!(ok = wait_pfree())) break;
+                if (jj == 0 && uit > 0) {
+                  // The previous unit's O left through this buffer: its tensor
+                  // stores must have read it.
+                  if (lane == 0) bulk_wait_read_all();
+                  __syncwarp();
+                }
+              }
+#pragma unroll
+              for (int c = 4 * hf; c < 4 * hf + 4; ++c)
+                st_shared_v4(prow + ((c ^ (r & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
+                             pk[4 * c + 3]);
             }
+            fence_proxy_async_smem();   // generic-proxy writes -> the MMA's operand reads
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(ctl.p_ready[t][0]));
+            ++np;
+            if (!ok) break;
           }
           ell += e_sum;
         } else {
           // p = 2^(s*c - m) against the running reference max m, so no
           // exponential waits for the block's max.  The block's sum of p bounds
-          // every p in it: if the sum is at most 2^8 the pass stands (p <= 2^8,
-          // as the reference rule requires).  Otherwise (rare after the
-          // first block: the block's max is then more than 1 above m) m moves to
-          // the block's max, O and the sums are rescaled and the block (still in
-          // registers; P is not signalled yet) is taken again.  P is rounded to
+          // every p in it: if the sum is at most 2^32 the pass stands (p <= 2^32;
+          // bf16 P and the f32 sums have the range for it, and their relative
+          // precision does not depend on the reference).  Otherwise (rare after
+          // the first block: the block's max is then more than 25 above m) m
+          // moves to the block's max, O and the sums are rescaled and the block
+          // (still in registers; P is not signalled yet) is taken again.  P is rounded to
           // bf16 for the PV MMA; the sum of exactly those rounded values (l~)
           // normalises O, so numerator and denominator use the same weights,
           // while the sum of the f32 values (l) gives the logsumexp.
@@ -763,8 +898,8 @@ __global__ void __launch_bounds__(384, 1)
           exps_half(x, 1, es1, rs1);
           e_sum = es0 + es1;
           r_sum = rs0 + rs1;
-          // A sum of 128 terms above 2^8 = 256 has a term above 2; moving m to
-          // the block's max makes every term <= 1, so one more pass suffices.
+          // A sum of 128 terms above 2^32 has a term above 2^25; moving m to the
+          // block's max makes every term <= 1, so one more pass suffices.
           const bool redo = !(e_sum <= C::kSumLimit);
           if (__any_sync(0xffffffffu, redo)) {
             const float m_blk = row_max(x) * cj;

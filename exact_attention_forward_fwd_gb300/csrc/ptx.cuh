@@ -62,6 +62,19 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 }
 
 // True once the phase with the given parity has completed.
+// Non-blocking probe of a phase (never suspends the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -396,6 +409,26 @@ __device__ __forceinline__ void mma_ss_x4_w(uint32_t d_tmem, uint64_t a0, uint64
         "@e tcgen05.mma.cta_group::1." GB300_MMA_KIND_F16 " [%0], %4, %8, %9, q;\n\t}\n" ::"r"(d_tmem),
         "l"(a0), "l"(a1), "l"(a2), "l"(a3), "l"(b0), "l"(b1), "l"(b2), "l"(b3), "r"(idesc),
         "r"(accumulate));
+  }
+}
+
+template <bool F8>
+__device__ __forceinline__ void mma_ss_x2_w(uint32_t d_tmem, uint64_t a0, uint64_t a1, uint64_t b0,
+                                            uint64_t b1, uint32_t idesc, uint32_t accumulate) {
+  if constexpr (F8) {
+    asm volatile(
+        "{\n\t.reg .pred p, q, e;\n\tsetp.ne.b32 p, %6, 0;\n\tsetp.eq.b32 q, %5, %5;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1." GB300_MMA_KIND_F8 " [%0], %1, %3, %5, p;\n\t"
+        "@e tcgen05.mma.cta_group::1." GB300_MMA_KIND_F8 " [%0], %2, %4, %5, q;\n\t}\n" ::"r"(d_tmem),
+        "l"(a0), "l"(a1), "l"(b0), "l"(b1), "r"(idesc), "r"(accumulate));
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p, q, e;\n\tsetp.ne.b32 p, %6, 0;\n\tsetp.eq.b32 q, %5, %5;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1." GB300_MMA_KIND_F16 " [%0], %1, %3, %5, p;\n\t"
+        "@e tcgen05.mma.cta_group::1." GB300_MMA_KIND_F16 " [%0], %2, %4, %5, q;\n\t}\n" ::"r"(d_tmem),
+        "l"(a0), "l"(a1), "l"(b0), "l"(b1), "r"(idesc), "r"(accumulate));
   }
 }
 
