@@ -172,11 +172,11 @@ def _time_loop(fn, steps, stream):
     return e0.elapsed_time(e1) / steps   # ms per step
 
 
-def _time_loop_flushed(fn, steps, stream, flush):
-    """Mean ms of fn over `steps` launches, each timed alone after a write of
+def _flushed_times(fn, steps, stream, flush):
+    """ms of fn for each of `steps` launches, each timed alone after a write of
     `flush` (larger than L2) so that no launch finds its inputs in L2."""
     import torch
-    total = 0.0
+    out = []
     for _ in range(steps):
         flush.zero_()
         e0 = torch.cuda.Event(enable_timing=True)
@@ -185,8 +185,8 @@ def _time_loop_flushed(fn, steps, stream, flush):
         fn()
         e1.record(stream)
         e1.synchronize()
-        total += e0.elapsed_time(e1)
-    return total / steps
+        out.append(e0.elapsed_time(e1))
+    return out
 
 
 def _oracle_run(q, k, v, w, heads, threads):
@@ -206,6 +206,65 @@ def _oracle_run(q, k, v, w, heads, threads):
         list(ex.map(lambda j: oa.three_pass_rows(*slices[(j[0], j[1])], w.scale, w.causal, j[2]),
                     jobs))
     return time.perf_counter() - t0, flops
+
+
+def _oracle_full(q, k, v, w, threads):
+    """The float64 oracle on every row of every head of the workload (CPU bf16
+    tensors), threaded over (b, h, 256-row chunks).  Returns (O, lse, seconds)."""
+    import numpy as np
+    from oracle import attention as oa
+    f64 = lambda t: t.float().numpy().astype(np.float64)
+    group = w.H // w.kv_heads
+    qs = {(b, h): f64(q[b, h]) for b in range(w.B) for h in range(w.H)}
+    kvs = {(b, g): (f64(k[b, g]), f64(v[b, g])) for b in range(w.B) for g in range(w.kv_heads)}
+    O = np.zeros((w.B, w.H, w.N, w.d))
+    L = np.zeros((w.B, w.H, w.N))
+    rows = np.arange(w.N)
+    jobs = [(b, h, rows[i:i + 256]) for b in range(w.B) for h in range(w.H)
+            for i in range(0, w.N, 256)]
+
+    def one(j):
+        b, h, r = j
+        kk, vv = kvs[(b, h // group)]
+        o, l = oa.three_pass_rows(qs[(b, h)], kk, vv, w.scale, w.causal, r, w.window)
+        O[b, h, r[0]:r[-1] + 1] = o
+        L[b, h, r[0]:r[-1] + 1] = l
+
+    t0 = time.perf_counter()
+    with concurrent.futures.ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(one, jobs))
+    return O, L, time.perf_counter() - t0
+
+
+def _errors(o, lse, O_ref, L_ref, fp8=False):
+    """Error statistics of a GPU result against the oracle (all rows)."""
+    import numpy as np
+    o = o.float().cpu().numpy().astype(np.float64)
+    lse = lse.float().cpu().numpy().astype(np.float64)
+    err = np.abs(o - O_ref)
+    out = {"max_abs": float(err.max()), "mean_abs": float(err.mean()),
+           "rmse": float(np.sqrt((err ** 2).mean())),
+           "rel_rmse": float(np.sqrt((err ** 2).mean() / (O_ref ** 2).mean())),
+           "lse_max_abs": float(np.abs(lse - L_ref).max()), "rows": "all"}
+    if not fp8:
+        import torch
+        Ob = torch.from_numpy(O_ref).to(torch.bfloat16).double().numpy()
+        out["bf16_rounding_floor_mean_abs"] = float(np.abs(Ob - O_ref).mean())
+        out["gates"] = "max abs <= 1e-2 beyond bf16 output rounding, mean abs <= 1e-3, lse <= 1e-3"
+    else:
+        out["gates"] = "rmse <= 3e-2 against the oracle on the unquantised inputs"
+    return out
+
+
+def _ideal_bytes(w):
+    """Q, K, V read once, O and lse written once (FP8: 1-byte operands and the
+    three tensors' block scales)."""
+    q_el = w.B * w.H * w.N * w.d
+    kv_el = w.B * w.kv_heads * w.N * w.d
+    if w.dtype == "fp8":
+        nblk = -(-w.N // 128)
+        return q_el + 2 * kv_el + 2 * q_el + 4 * w.B * w.H * w.N + 3 * 4 * w.B * w.H * nblk
+    return 2 * (q_el + 2 * kv_el) + 2 * q_el + 4 * w.B * w.H * w.N
 
 
 def run_reference(args):
@@ -281,6 +340,13 @@ def run_mine(args):
     ms = mor(ms)
     tflops_launch = w.flops / (ms * 1e-3) / 1e12
     value = whole_job_tflops(w.flops, ms, ws)
+    # The same launch timed alone after an L2 flush (a 256 MiB write), median
+    # of at least 20: the method the scope table states, next to the mean of
+    # back-to-back launches above.
+    flush0 = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    ts_main = _flushed_times(step, max(20, args.steps), stream, flush0)
+    del flush0
+    ms_flushed = mor(statistics.median(ts_main))
 
     # ---------------------------------------------------------------- e2e
     # End to end through the public API: every step uploads its Q, K, V from
@@ -346,6 +412,8 @@ def run_mine(args):
     del qb[1], kb[1], vb[1], ob[1], lb[1]
 
     # ---------------------------------------------------------------- FP8
+    # Prep + attention and prep alone, back to back (the per-config section
+    # below times the attention alone with L2 flushed and checks its errors).
     fp8 = None
     if not args.no_extra:
         wf = inputs.WORKLOADS["fp8_n8192_d128"]
@@ -359,16 +427,14 @@ def run_mine(args):
         attn8 = lambda: ga.attn_fwd_fp8(q8, k8, v8, sq, sk, sv, causal=wf.causal, scale=wf.scale,
                                         out=of, lse=lf)
 
-        def full8():
-            ga.fp8_prep(fq, signs, out=q8, scales=sq)
-            ga.fp8_prep(fk, signs, out=k8, scales=sk)
-            ga.fp8_prep(fv, None, transpose=True, out=v8, scales=sv)
-            attn8()
-
         def prep8():
             ga.fp8_prep(fq, signs, out=q8, scales=sq)
             ga.fp8_prep(fk, signs, out=k8, scales=sk)
             ga.fp8_prep(fv, None, transpose=True, out=v8, scales=sv)
+
+        def full8():
+            prep8()
+            attn8()
 
         for _ in range(args.warmup):
             full8()
@@ -422,20 +488,35 @@ def run_mine(args):
             raise RuntimeError("kernel status word set during the backward benchmark")
         del dO, dq, dk, dv, wsb
 
-    # ------------------------------------------------------- other workloads
+    # ------------------------------------------------------- per workload
+    # Every workload of the catalogue: each launch timed alone after a 256 MiB
+    # write that flushes L2 (median of the launches), the fraction of the
+    # tensor peak, ideal HBM bytes against those ncu measured (where a summary
+    # taken on the current kernel source exists), and the errors against the
+    # float64 oracle over every row, with the oracle's own wall time.
     others = {}
     if not args.no_extra:
-        # Each launch is timed alone after a 256 MiB write that flushes L2 (some
-        # of these workloads fit in L2).
         flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
-        for name in ("n8192_d128_causal", "n32768_d64_causal", "n2048_d128", "n2048_d128_causal",
-                     "n8192_d128_gqa4_window4096", "n8192_d128_b1h2", "n8192_d128_b1h2_causal"):
+        threads = os.cpu_count() or 1
+        for name in ("n256_d64", "n2048_d128", "n2048_d128_causal", "n2048_d128_k8",
+                     "n2048_d128_k8_causal", "n8192_d128", "n8192_d128_causal",
+                     "n32768_d64_causal", "fp8_n8192_d128", "n8192_d128_gqa4_window4096",
+                     "n8192_d128_b1h2", "n8192_d128_b1h2_causal"):
             wo = inputs.WORKLOADS[name]
-            a, b, c = (t.to(dev) for t in inputs.workload_inputs(wo))
+            qh_, kh_, vh_ = inputs.workload_inputs(wo)
+            a, b, c = qh_.to(dev), kh_.to(dev), vh_.to(dev)
             oo = torch.empty_like(a)
             lo = torch.empty(wo.B, wo.H, wo.N, dtype=torch.float32, device=dev)
-            if wo.H_kv or wo.window:
+            is8 = wo.dtype == "fp8"
+            if is8:
+                sg = inputs.make_signs(wo.H, wo.d, wo.seed).to(dev)
+                a8, sa = ga.fp8_prep(a, sg)
+                b8, sb = ga.fp8_prep(b, sg)
+                c8, sc = ga.fp8_prep(c, None, transpose=True)
+                fn = lambda: ga.attn_fwd_fp8(a8, b8, c8, sa, sb, sc, causal=wo.causal,
+                                             scale=wo.scale, out=oo, lse=lo)
+            elif wo.H_kv or wo.window:
                 fn = lambda: ga.attn_fwd_ex(a, b, c, causal=wo.causal, window=wo.window,
                                             scale=wo.scale, out=oo, lse=lo)
             else:
@@ -443,9 +524,20 @@ def run_mine(args):
             for _ in range(args.warmup):
                 fn()
             barrier()
-            mso = mor(_time_loop_flushed(fn, args.steps, stream, flush))
-            others[name] = {"tflops": wo.flops / (mso * 1e-3) / 1e12 * ws, "ms": mso,
-                            "l2": "flushed before each launch"}
+            ts = _flushed_times(fn, max(20, args.steps), stream, flush)
+            msm = mor(statistics.median(ts))
+            tfl = wo.flops / (msm * 1e-3) / 1e12
+            peak = (2 if is8 else 1) * peaks["bf16"]
+            kern = f"attn_fwd_{'fp8' if is8 else 'bf16'}_d{wo.d}_{wo.name}"
+            entry = {"tflops": tfl * ws, "ms_median": msm, "ms_mean": mor(statistics.fmean(ts)),
+                     "launches": len(ts), "l2": "flushed before each launch",
+                     "roofline": {"bound": "tensor", "achieved": tfl, "peak": peak,
+                                  "unit": "TFLOP/s", "frac": tfl / peak,
+                                  "peak_note": "measured bf16 burst" + (" x 2" if is8 else "")},
+                     "hbm": {"ideal_bytes": _ideal_bytes(wo),
+                             "dram_bytes_ncu": _profiled_traffic(kern)}}
+            if entry["hbm"]["dram_bytes_ncu"]:
+                entry["hbm"]["ratio"] = entry["hbm"]["dram_bytes_ncu"] / entry["hbm"]["ideal_bytes"]
             if name.startswith("n8192_d128_b1h2"):
                 # Split-KV on the same inputs, with the library's default split count.
                 S = ga.splitkv_default_splits(wo.B, wo.H, wo.N, wo.d, wo.causal, sms)
@@ -456,11 +548,22 @@ def run_mine(args):
                 for _ in range(args.warmup):
                     fs()
                 barrier()
-                mss = mor(_time_loop_flushed(fs, args.steps, stream, flush))
-                others[name]["splitkv"] = {"tflops": wo.flops / (mss * 1e-3) / 1e12 * ws,
-                                           "ms": mss, "splits": S, "launches_per_call": 2}
+                mss = mor(statistics.median(_flushed_times(fs, max(20, args.steps), stream, flush)))
+                entry["splitkv"] = {"tflops": wo.flops / (mss * 1e-3) / 1e12 * ws,
+                                    "ms_median": mss, "splits": S, "launches_per_call": 2}
                 del wsp
+            if rank == 0 and not args.no_cpu_baseline:
+                fn()
+                torch.cuda.synchronize(dev)
+                O_ref, L_ref, secs = _oracle_full(qh_, kh_, vh_, wo, threads)
+                entry["errors"] = _errors(oo, lo, O_ref, L_ref, fp8=is8)
+                entry["oracle"] = {"seconds": secs, "cores": threads, "rows": "all",
+                                   "tflops": wo.flops / secs / 1e12}
+                del O_ref, L_ref
+            others[name] = entry
             del a, b, c, oo, lo
+            if is8:
+                del a8, b8, c8
         del flush
         barrier()
     if ga.device_status() != 0:
@@ -508,6 +611,8 @@ def run_mine(args):
             "roofline": {"bound": "tensor", "achieved": tflops_launch, "peak": peaks["bf16"],
                          "unit": "TFLOP/s", "frac": tflops_launch / peaks["bf16"],
                          "traffic": traffic, "peak_source": peaks["source"] + " bf16 burst"},
+            "timing_l2_flushed": {"ms_median": ms_flushed, "launches": len(ts_main),
+                                  "tflops": whole_job_tflops(w.flops, ms_flushed, ws)},
             "e2e": {"value": w.flops / (ms_e2e * 1e-3) / 1e12 * ws, "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e,
                     "steps": n_e2e, "pipelined": "2 buffer sets, upload/compute/download streams"},
