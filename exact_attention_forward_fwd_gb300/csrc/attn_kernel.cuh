@@ -137,6 +137,12 @@ struct KCfg {
   // memory, so a tile's next S product can start as soon as its softmax has
   // read S, and P.V reads P as an SS operand.
   static constexpr bool kPSmem = FP8;
+  // bf16 at d = 64: P has TMEM columns of its own (the 128 that d = 64 leaves
+  // free: tile t at [256 + 2D + 64 t, +64)), so S_t(j+1) need not wait for
+  // P_t(j).V either.  Both forms take the decoupled issue order below.
+  static constexpr bool kPSep = !FP8 && D == 64;
+  static constexpr bool kDecoupled = kPSmem || kPSep;
+  static constexpr uint32_t kPCol = 256 + 2 * D;
   static constexpr int kSKSteps = FP8 ? D / 32 : D / 16;  // k-steps of S = Q K^T
   static constexpr int kPVSteps = FP8 ? 4 : 8;            // k-steps of O += P V (128 keys)
   static constexpr uint32_t kIdescS =
@@ -459,13 +465,14 @@ __global__ void __launch_bounds__(384, 1)
       auto wait_item = [&](uint32_t it) {
         return wait_w(ctl.kv_full[it % C::kStages], (it / C::kStages) & 1);
       };
-      if constexpr (C::kPSmem) {
-        // FP8, P in shared memory.  S_t(j+1) is issued once the softmax has
-        // read S_t(j) (s_free) and K_{j+1} has landed; P_t(j).V_j once both
-        // halves of P_t(j) are in shared memory.  A tile's softmax therefore
-        // never waits for its own products: the next S is computed while it
-        // works on the current block.  p_free (a commit after each P.V) tells
-        // the softmax that the P buffer may be refilled and O rescaled.
+      if constexpr (C::kDecoupled) {
+        // P outside the S columns (FP8: shared memory; bf16 d = 64: TMEM
+        // columns of its own).  S_t(j+1) is issued once the softmax has read
+        // S_t(j) (s_free) and K_{j+1} has landed; P_t(j).V_j once P_t(j) is
+        // stored.  A tile's softmax therefore never waits for its own
+        // products: the next S is computed while it works on the current
+        // block.  p_free (a commit after each P.V) tells the softmax that the
+        // P buffer may be refilled and O rescaled.
         uint32_t ns[2] = {0, 0};   // S products issued per tile
         uint32_t npv = 0;          // P.V products issued per tile
         const uint64_t dP = make_smem_desc(sO, 16, 1024, kSwizzle128B);
@@ -477,15 +484,29 @@ __global__ void __launch_bounds__(384, 1)
           mma_commit_w(bar(ctl.s_full[t]));
           return true;
         };
-        // O_t (+)= P_t V over the block's 128 keys (four K = 32 steps) once
-        // P_t is in shared memory.
+        // O_t (+)= P_t V over the block's 128 keys once P_t is stored: FP8,
+        // four K = 32 steps with P from shared memory; bf16, eight K = 16
+        // steps with P from its TMEM columns (16 keys = 8 columns per step,
+        // V rows 2048 bytes apart).
         auto issue_pv = [&](int t, uint32_t vslot, bool acc) -> bool {
-          const uint64_t da = dP + t * (uint64_t)(C::kOStageBytes >> 4);
           const uint64_t db = dV + vslot * kTileUnits;
           if (!wait_w(ctl.p_ready[t][0], npv & 1)) return false;
           tc_fence_after();
-          mma_ss_x4_w<true>(tmem + 256 + D * t, da, da + 2, da + 4, da + 6, db, db + 2, db + 4,
-                            db + 6, C::kIdescPV, acc ? 1u : 0u);
+          if constexpr (FP8) {
+            const uint64_t da = dP + t * (uint64_t)(C::kOStageBytes >> 4);
+            mma_ss_x4_w<true>(tmem + 256 + D * t, da, da + 2, da + 4, da + 6, db, db + 2, db + 4,
+                              db + 6, C::kIdescPV, acc ? 1u : 0u);
+          } else {
+            const uint32_t ta = tmem + C::kPCol + 64 * t;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+              const int k = 4 * hf;
+              mma_ts_x4_w<false>(tmem + 256 + D * t, ta + k * 8, ta + k * 8 + 8, ta + k * 8 + 16,
+                                 ta + k * 8 + 24, db + k * 128, db + k * 128 + 128,
+                                 db + k * 128 + 256, db + k * 128 + 384, C::kIdescPV,
+                                 (acc || hf > 0) ? 1u : 0u);
+            }
+          }
           mma_commit_w(bar(ctl.p_free[t]));
           return true;
         };
@@ -607,6 +628,8 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + lane_off + 128 * t;
     const uint32_t tO = tmem + lane_off + 256 + D * t;
+    // bf16 P: over S (d = 128), or in its own columns (d = 64).
+    const uint32_t tP = C::kPSep ? tmem + lane_off + C::kPCol + 64 * t : tS;
     const float NEG_INF = __int_as_float(0xff800000);
     const bool zero_scale = p.zero_scale != 0;
     uint32_t sit = 0, uit = 0;
@@ -690,6 +713,18 @@ __global__ void __launch_bounds__(384, 1)
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
+        // With P outside the S columns, the previous block's P.V must be done
+        // before O_t is rescaled or the P buffer refilled (it was issued as
+        // that block's P landed, so this is rarely a wait).
+        bool pfree = np == 0;
+        auto wait_pfree = [&]() {
+          if (pfree) return true;
+          pfree = true;
+          const uint32_t pb = bar(ctl.p_free[t]), ph = (np - 1) & 1;
+          const bool w_ok = __all_sync(0xffffffffu, mbar_test_wait(pb, ph) || wait_bounded(pb, ph, wc));
+          tc_fence_after();
+          return w_ok;
+        };
         const int lim = lim_row - j * 128;    // columns > lim are invisible
         const int lo = lo_row - j * 128;      // columns < lo are invisible (window)
         // S of this block -> x (raw scores; invisible columns -inf).
@@ -781,18 +816,6 @@ __global__ void __launch_bounds__(384, 1)
             const bool need = m_blk > m_ref + C::kTauLog2;
             const float m_new = need ? m_blk : m_ref;
             const float alpha = need ? ex2_approx(m_ref - m_new) : 1.0f;   // 0 when m_ref = -inf
-            // The previous block's P.V must be done before O_t is rescaled or
-            // the P buffer refilled (it was issued as that block's P landed).
-            bool pfree = np == 0;
-            auto wait_pfree = [&]() {
-              if (pfree) return true;
-              pfree = true;
-              const uint32_t pb = bar(ctl.p_free[t]), ph = (np - 1) & 1;
-              const bool w_ok =
-                  __all_sync(0xffffffffu, mbar_test_wait(pb, ph) || wait_bounded(pb, ph, wc));
-              tc_fence_after();
-              return w_ok;
-            };
             if (jj > 0 && __any_sync(0xffffffffu, need)) {
               if (!(ok = wait_pfree())) break;
               rescale_o(alpha);
@@ -887,14 +910,23 @@ __global__ void __launch_bounds__(384, 1)
           // nothing is rescaled.
           float x[128];
           load_s(x);
+          if constexpr (C::kPSep) {
+            // S is in registers now: the tile's next S product may overwrite it.
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(ctl.s_free[t]));
+          }
           if (!__all_sync(0xffffffffu, m_ref != NEG_INF)) {
             const float m_blk0 = row_max(x) * cj;
             if (m_ref == NEG_INF) m_ref = m_blk0;
           }
           float es0, rs0, es1, rs1;
           exps_half(x, 0, es0, rs0);
+          if constexpr (C::kPSep) {
+            if (!(ok = wait_pfree())) break;
+          }
           __syncwarp();   // tcgen05.st is warp-collective
-          tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+          tmem_st32(tP, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
           exps_half(x, 1, es1, rs1);
           e_sum = es0 + es1;
           r_sum = rs0 + rs1;
@@ -914,14 +946,15 @@ __global__ void __launch_bounds__(384, 1)
             e_sum = es0 + es1;
             r_sum = rs0 + rs1;
             __syncwarp();
-            tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+            tmem_st32(tP, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
           }
           __syncwarp();   // tcgen05.st is warp-collective
-          tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+          tmem_st32(tP + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
           // bf16: one signal for all keys of the block (P·V waits for it once).
           tmem_wait_st();
           tc_fence_before();
           mbar_arrive(bar(ctl.p_ready[t][0]));
+          if constexpr (C::kPSep) ++np;
           ell_r += r_sum;
           ell += e_sum;
         }
