@@ -164,7 +164,7 @@ struct SmemCtl {
   uint64_t drain;
   uint64_t unit_full[4];    // ring of work-unit indices handed out by the load warp
   uint64_t unit_empty[4];
-  int unit_ring[4];
+  int4 unit_ring[4][2];     // decoded work units (Unit fields; valid = 0 ends)
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -312,26 +312,39 @@ __global__ void __launch_bounds__(384, 1)
   const WaitCtx wc{&ctl.abort_flag, p.status ? p.status : &g_attn_status, p.timeout_ns};
 
   // Work units: the load warp takes the next index (atomic counter, or the
-  // static stride without one) and passes it through a 4-entry ring; -1 ends.
-  auto publish_unit = [&](uint32_t k, bool& ok) -> int {
+  // static stride without one), decodes it once (unit_of divides by runtime
+  // values: hundreds of cycles of latency that every role would otherwise pay
+  // at each unit boundary) and passes the decoded unit through a 4-entry
+  // ring; an entry with valid = 0 ends the kernel.
+  auto publish_unit = [&](uint32_t k, bool& ok, Unit& w) -> int {
     int u = p.sched ? atomicAdd(p.sched, 1) : static_cast<int>(blockIdx.x + k * gridDim.x);
     if (u >= p.num_units) u = -1;
+    if (u >= 0) w = unit_of(u, p);
     const uint32_t slot = k & 3;
     if (k >= 4 && !(ok = wait_bounded(bar(ctl.unit_empty[slot]), ((k >> 2) - 1) & 1, wc))) return -1;
-    ctl.unit_ring[slot] = u;
+    ctl.unit_ring[slot][0] = make_int4(w.bh, w.bhk, w.pair, w.j0);
+    ctl.unit_ring[slot][1] = make_int4(w.nblocks, w.split, w.skip0 ? 1 : 0, u >= 0 ? 1 : 0);
     mbar_arrive(bar(ctl.unit_full[slot]));
     return u;
   };
-  // Consumer side (a whole warp; lane 0 frees the slot).
-  auto take_unit = [&](uint32_t k, bool& ok) -> int {
+  // Consumer side (a whole warp; lane 0 frees the slot).  Returns false at the end.
+  auto take_unit = [&](uint32_t k, bool& ok, Unit& w) -> bool {
     const uint32_t slot = k & 3;
     ok = wait_bounded(bar(ctl.unit_full[slot]), (k >> 2) & 1, wc);
     ok = __all_sync(0xffffffffu, ok);
-    if (!ok) return -1;
-    const int u = *reinterpret_cast<volatile int*>(&ctl.unit_ring[slot]);
+    if (!ok) return false;
+    const int4 a = ld_shared_v4_s32(smem_addr(&ctl.unit_ring[slot][0]));
+    const int4 b = ld_shared_v4_s32(smem_addr(&ctl.unit_ring[slot][1]));
     __syncwarp();
     if (lane == 0) mbar_arrive(bar(ctl.unit_empty[slot]));
-    return u;
+    w.bh = a.x;
+    w.bhk = a.y;
+    w.pair = a.z;
+    w.j0 = a.w;
+    w.nblocks = b.x;
+    w.split = b.y;
+    w.skip0 = b.z != 0;
+    return b.w != 0;
   };
 
   // Each role sets its warpgroup's register budget first (warps 8-11 give
@@ -351,9 +364,9 @@ __global__ void __launch_bounds__(384, 1)
       bool ok = true;
       int loads = 0;
       for (uint32_t k = 0; ok; ++k) {
-        const int u = publish_unit(k, ok);
+        Unit w{};
+        const int u = publish_unit(k, ok, w);
         if (u < 0) break;
-        const Unit w = unit_of(u, p);
         if (w.nblocks == 0) continue;   // empty key range (split-KV)
         // Warm L2 with this unit's Q tiles and first two key blocks while the
         // previous unit still runs: their loads wait for its buffers, and would
@@ -511,9 +524,8 @@ __global__ void __launch_bounds__(384, 1)
           return true;
         };
         for (uint32_t k = 0; ok; ++k) {
-          const int u = take_unit(k, ok);
-          if (u < 0) break;
-          const Unit w = unit_of(u, p);
+          Unit w{};
+          if (!take_unit(k, ok, w)) break;
           const int J = w.nblocks;
           if (J == 0) continue;
           ok = wait_w(ctl.q_full[0], uit & 1) && wait_w(ctl.q_full[1], uit & 1);
@@ -550,9 +562,8 @@ __global__ void __launch_bounds__(384, 1)
         }
       } else
       for (uint32_t k = 0; ok; ++k) {
-        const int u = take_unit(k, ok);
-        if (u < 0) break;
-        const Unit w = unit_of(u, p);
+        Unit w{};
+        if (!take_unit(k, ok, w)) break;
         const int J = w.nblocks;
         if (J == 0) continue;   // empty key range (split-KV)
         ok = wait_w(ctl.q_full[0], uit & 1) && wait_w(ctl.q_full[1], uit & 1);
@@ -656,9 +667,8 @@ __global__ void __launch_bounds__(384, 1)
       __syncwarp();
     };
     for (uint32_t k = 0; ok; ++k) {
-      const int u = take_unit(k, ok);
-      if (u < 0) break;
-      const Unit w = unit_of(u, p);
+      Unit w{};
+      if (!take_unit(k, ok, w)) break;
       const int row = w.pair * 256 + t * 128 + r;
       if (w.nblocks == 0) {
         // Empty key range: O_part = 0 and lse_part = -inf (weight 0 in the merge).
@@ -1024,13 +1034,26 @@ __global__ void __launch_bounds__(384, 1)
         if constexpr (D == 128) {
           const uint32_t wstage = sO + t * C::kOStageBytes + wq * 4096;
           const int wrow0 = w.pair * 256 + t * 128 + wq * 32;
-#pragma unroll 1
+          // All 128 columns of the row in one TMEM round trip (the softmax's
+          // registers are free here), then the two 64-column slabs through
+          // the staging buffer one after the other.
+          uint32_t pk[2][32];
+          {
+            uint32_t ov[128];
+            __syncwarp();
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld32(tO + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&ov[32 * c]));
+            tmem_wait_ld();
+            reg_fence(ov);
+#pragma unroll
+            for (int i = 0; i < 64; ++i)
+              pk[i >> 5][i & 31] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv, __uint_as_float(ov[2 * i + 1]) * inv);
+          }
+#pragma unroll
           for (int sl = 0; sl < 2; ++sl) {
-            uint32_t pk[32];
-            load_o_bf16(64 * sl, inv, pk);
             if (lane == 0) bulk_wait_read_all();
             __syncwarp();
-            stage_row(wstage + lane * 128, lane, pk);
+            stage_row(wstage + lane * 128, lane, pk[sl]);
             if (lane == 0 && wrow0 < p.N) {
               tma_store_3d(&tmO, wstage, 64 * sl, wrow0, w.bh);
               bulk_commit();

@@ -62,6 +62,16 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 }
 
 // True once the phase with the given parity has completed.
+// 16-byte shared-memory load (a volatile asm: not merged with earlier loads).
+__device__ __forceinline__ int4 ld_shared_v4_s32(uint32_t addr) {
+  int4 v;
+  asm volatile("ld.shared.v4.s32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
 // Non-blocking probe of a phase (never suspends the thread).
 __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
