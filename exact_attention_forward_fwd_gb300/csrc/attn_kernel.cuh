@@ -740,10 +740,7 @@ __global__ void __launch_bounds__(384, 1)
         // S of this block -> x (raw scores; invisible columns -inf).
         auto load_s = [&](float (&x)[128]) {
           uint32_t sr[128];
-          tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-          tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-          tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
-          tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
+          tmem_ld128(tS, sr);
           tmem_wait_ld();
           reg_fence(sr);
 #pragma unroll
