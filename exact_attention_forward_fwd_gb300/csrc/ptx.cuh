@@ -61,7 +61,6 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                : "memory");
 }
 
-// True once the phase with the given parity has completed.
 // 16-byte shared-memory load (a volatile asm: not merged with earlier loads).
 __device__ __forceinline__ int4 ld_shared_v4_s32(uint32_t addr) {
   int4 v;
@@ -85,6 +84,8 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// True once the phase with the given parity has completed (the thread may be
+// suspended for a while inside the instruction first).
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
