@@ -157,9 +157,11 @@ struct SmemCtl {
   uint64_t q_full[2];
   uint64_t q_empty[2];
   uint64_t s_full[2];
-  uint64_t p_ready[2][2];   // [tile][half of the block's keys] (bf16 signals all keys on [t][0])
-  uint64_t s_free[2];       // FP8: the tile's S has been read (its TMEM columns may be overwritten)
-  uint64_t p_free[2];       // FP8: the tile's P.V is done (its P buffer may be overwritten)
+  uint64_t p_ready[2];      // [tile]: the block's P is stored
+  uint64_t s_free[2];       // decoupled order (FP8, d = 64): the tile's S has been read (its
+                            // TMEM columns may be overwritten)
+  uint64_t p_free[2];       // decoupled order: the tile's P.V is done (its P buffer may be
+                            // overwritten, O_t rescaled)
   uint64_t o_final[2];
   uint64_t drain;
   uint64_t unit_full[4];    // ring of work-unit indices handed out by the load warp
@@ -286,8 +288,7 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(bar(ctl.s_full[t]), 1);
       // FP8: one arrival per softmax warp of the tile (measured +1 %); bf16: one
       // per thread (a warp-level arrival after __syncwarp measured -2 % there).
-      mbar_init(bar(ctl.p_ready[t][0]), FP8 ? 4 : 128);
-      mbar_init(bar(ctl.p_ready[t][1]), FP8 ? 4 : 128);
+      mbar_init(bar(ctl.p_ready[t]), FP8 ? 4 : 128);
       mbar_init(bar(ctl.o_final[t]), 1);
       mbar_init(bar(ctl.s_free[t]), 4);
       mbar_init(bar(ctl.p_free[t]), 1);
@@ -457,23 +458,16 @@ __global__ void __launch_bounds__(384, 1)
                            db + o + 2, db + o + 4, db + o + 6, idesc_s, g > 0 ? 1u : 0u);
         }
       };
-      // O_t += P_t V over the keys of half `hf` of the block (P of each half is
-      // signalled separately, so the first half's product overlaps the
-      // exponentials of the second).
+      // bf16 with P over S (d = 128): O_t += P_t V over the keys of half `hf` of
+      // the block, P from the tile's S columns.
       auto pv_mma = [&](int t, uint32_t vslot, bool acc, int hf) {
         const uint64_t db = dV + vslot * kTileUnits;
         const uint32_t ta = tmem + 128 * t;
         const uint32_t acc0 = (acc || hf > 0) ? 1u : 0u;
-        if constexpr (FP8) {
-          const int k = 2 * hf;
-          mma_f8_ts_w(tmem + 256 + D * t, ta + k * 8, db + k * 2, C::kIdescPV, acc0);
-          mma_f8_ts_w(tmem + 256 + D * t, ta + k * 8 + 8, db + k * 2 + 2, C::kIdescPV, 1u);
-        } else {
-          const int k = 4 * hf;   // 16-key steps: P columns advance by 8, V rows by 2048 bytes
-          mma_ts_x4_w<false>(tmem + 256 + D * t, ta + k * 8, ta + k * 8 + 8, ta + k * 8 + 16,
-                             ta + k * 8 + 24, db + k * 128, db + k * 128 + 128, db + k * 128 + 256,
-                             db + k * 128 + 384, C::kIdescPV, acc0);
-        }
+        const int k = 4 * hf;   // 16-key steps: P columns advance by 8, V rows by 2048 bytes
+        mma_ts_x4_w<false>(tmem + 256 + D * t, ta + k * 8, ta + k * 8 + 8, ta + k * 8 + 16,
+                           ta + k * 8 + 24, db + k * 128, db + k * 128 + 128, db + k * 128 + 256,
+                           db + k * 128 + 384, C::kIdescPV, acc0);
       };
       auto wait_item = [&](uint32_t it) {
         return wait_w(ctl.kv_full[it % C::kStages], (it / C::kStages) & 1);
@@ -503,7 +497,7 @@ __global__ void __launch_bounds__(384, 1)
         // V rows 2048 bytes apart).
         auto issue_pv = [&](int t, uint32_t vslot, bool acc) -> bool {
           const uint64_t db = dV + vslot * kTileUnits;
-          if (!wait_w(ctl.p_ready[t][0], npv & 1)) return false;
+          if (!wait_w(ctl.p_ready[t], npv & 1)) return false;
           tc_fence_after();
           if constexpr (FP8) {
             const uint64_t da = dP + t * (uint64_t)(C::kOStageBytes >> 4);
@@ -587,12 +581,10 @@ __global__ void __launch_bounds__(384, 1)
           const uint32_t vslot = iv % C::kStages, kslot = ik % C::kStages;
           if (!(ok = wait_item(iv))) break;
           if (j < J0) {
-            if (!(ok = wait_w(ctl.p_ready[0][0], pr[0] & 1))) break;
+            if (!(ok = wait_w(ctl.p_ready[0], pr[0] & 1))) break;
             tc_fence_after();
             pv_mma(0, vslot, j > 0, 0);
-            if (FP8 && !(ok = wait_w(ctl.p_ready[0][1], pr[0] & 1))) break;
             ++pr[0];
-            tc_fence_after();
             pv_mma(0, vslot, j > 0, 1);
             if (j == J0 - 1) mma_commit_w(bar(ctl.o_final[0]));
           }
@@ -604,12 +596,10 @@ __global__ void __launch_bounds__(384, 1)
               mma_commit_w(bar(ctl.s_full[0]));
             }
           }
-          if (!(ok = wait_w(ctl.p_ready[1][0], pr[1] & 1))) break;
+          if (!(ok = wait_w(ctl.p_ready[1], pr[1] & 1))) break;
           tc_fence_after();
           pv_mma(1, vslot, j > 0, 0);
-          if (FP8 && !(ok = wait_w(ctl.p_ready[1][1], pr[1] & 1))) break;
           ++pr[1];
-          tc_fence_after();
           pv_mma(1, vslot, j > 0, 1);
           mma_commit_w(bar(ctl.kv_empty[vslot]));
           if (j == J - 1) mma_commit_w(bar(ctl.o_final[1]));
@@ -857,7 +847,7 @@ __global__ void __launch_bounds__(384, 1)
             }
             fence_proxy_async_smem();   // generic-proxy writes -> the MMA's operand reads
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(ctl.p_ready[t][0]));
+            if (lane == 0) mbar_arrive(bar(ctl.p_ready[t]));
             ++np;
             if (!ok) break;
           }
@@ -960,7 +950,7 @@ __global__ void __launch_bounds__(384, 1)
           // bf16: one signal for all keys of the block (P·V waits for it once).
           tmem_wait_st();
           tc_fence_before();
-          mbar_arrive(bar(ctl.p_ready[t][0]));
+          mbar_arrive(bar(ctl.p_ready[t]));
           if constexpr (C::kPSep) ++np;
           ell_r += r_sum;
           ell += e_sum;
