@@ -142,6 +142,12 @@ struct KCfg {
   // P_t(j).V either.  Both forms take the decoupled issue order below.
   static constexpr bool kPSep = !FP8 && D == 64;
   static constexpr bool kDecoupled = kPSmem || kPSep;
+  // Tile t's P-ready barrier is p_ready[t * kPReadyStride].  Neither the
+  // spacing nor the spare word between the bf16 barriers carries a signal;
+  // both are what measured fastest (same-box A/B, three repeats): FP8 1.6 %
+  // faster with its two barriers adjacent, bf16 d = 128 1 % faster with them
+  // 16 bytes apart and the word between them initialised as a barrier too.
+  static constexpr int kPReadyStride = FP8 ? 1 : 2;
   static constexpr uint32_t kPCol = 256 + 2 * D;
   static constexpr int kSKSteps = FP8 ? D / 32 : D / 16;  // k-steps of S = Q K^T
   static constexpr int kPVSteps = FP8 ? 4 : 8;            // k-steps of O += P V (128 keys)
@@ -157,7 +163,7 @@ struct SmemCtl {
   uint64_t q_full[2];
   uint64_t q_empty[2];
   uint64_t s_full[2];
-  uint64_t p_ready[2];      // [tile]: the block's P is stored
+  uint64_t p_ready[4];      // tile t at [t * kPReadyStride]
   uint64_t s_free[2];       // decoupled order (FP8, d = 64): the tile's S has been read (its
                             // TMEM columns may be overwritten)
   uint64_t p_free[2];       // decoupled order: the tile's P.V is done (its P buffer may be
@@ -288,7 +294,8 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(bar(ctl.s_full[t]), 1);
       // FP8: one arrival per softmax warp of the tile (measured +1 %); bf16: one
       // per thread (a warp-level arrival after __syncwarp measured -2 % there).
-      mbar_init(bar(ctl.p_ready[t]), FP8 ? 4 : 128);
+      mbar_init(bar(ctl.p_ready[t * C::kPReadyStride]), FP8 ? 4 : 128);
+      if (!FP8) mbar_init(bar(ctl.p_ready[t * C::kPReadyStride + 1]), 128);
       mbar_init(bar(ctl.o_final[t]), 1);
       mbar_init(bar(ctl.s_free[t]), 4);
       mbar_init(bar(ctl.p_free[t]), 1);
@@ -497,7 +504,7 @@ __global__ void __launch_bounds__(384, 1)
         // V rows 2048 bytes apart).
         auto issue_pv = [&](int t, uint32_t vslot, bool acc) -> bool {
           const uint64_t db = dV + vslot * kTileUnits;
-          if (!wait_w(ctl.p_ready[t], npv & 1)) return false;
+          if (!wait_w(ctl.p_ready[t * C::kPReadyStride], npv & 1)) return false;
           tc_fence_after();
           if constexpr (FP8) {
             const uint64_t da = dP + t * (uint64_t)(C::kOStageBytes >> 4);
@@ -585,6 +592,7 @@ __global__ void __launch_bounds__(384, 1)
             tc_fence_after();
             pv_mma(0, vslot, j > 0, 0);
             ++pr[0];
+            tc_fence_after();
             pv_mma(0, vslot, j > 0, 1);
             if (j == J0 - 1) mma_commit_w(bar(ctl.o_final[0]));
           }
@@ -596,10 +604,11 @@ __global__ void __launch_bounds__(384, 1)
               mma_commit_w(bar(ctl.s_full[0]));
             }
           }
-          if (!(ok = wait_w(ctl.p_ready[1], pr[1] & 1))) break;
+          if (!(ok = wait_w(ctl.p_ready[C::kPReadyStride], pr[1] & 1))) break;
           tc_fence_after();
           pv_mma(1, vslot, j > 0, 0);
           ++pr[1];
+          tc_fence_after();
           pv_mma(1, vslot, j > 0, 1);
           mma_commit_w(bar(ctl.kv_empty[vslot]));
           if (j == J - 1) mma_commit_w(bar(ctl.o_final[1]));
@@ -847,7 +856,7 @@ __global__ void __launch_bounds__(384, 1)
             }
             fence_proxy_async_smem();   // generic-proxy writes -> the MMA's operand reads
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(ctl.p_ready[t]));
+            if (lane == 0) mbar_arrive(bar(ctl.p_ready[t * C::kPReadyStride]));
             ++np;
             if (!ok) break;
           }
@@ -950,7 +959,7 @@ __global__ void __launch_bounds__(384, 1)
           // bf16: one signal for all keys of the block (P·V waits for it once).
           tmem_wait_st();
           tc_fence_before();
-          mbar_arrive(bar(ctl.p_ready[t]));
+          mbar_arrive(bar(ctl.p_ready[t * C::kPReadyStride]));
           if constexpr (C::kPSep) ++np;
           ell_r += r_sum;
           ell += e_sum;
