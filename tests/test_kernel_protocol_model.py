@@ -20,7 +20,8 @@ Checked: every role finishes (no wait that never completes); every S product
 lands in a TMEM buffer whose previous S the softmax has already read; every
 P.V reads the P it is meant to, and no P is overwritten before its P.V read
 it; the K/V ring never refills a slot before its tile was consumed; every
-product of a unit is issued before the unit's output is read.  Mutations of
+product of a unit is issued before the unit's output is read; no S product
+reads a Q tile the next unit's copy has replaced.  Mutations of
 the protocol (a wait dropped, a wrong parity, a barrier shared by two P
 buffers) must be caught.
 """
@@ -67,6 +68,7 @@ def simulate(units, decoupled, stages, mutate=None, seed=0):
             bar((n, t))
     # Safety state: what each TMEM / shared buffer holds.
     ring = [None] * stages          # item index held by each ring slot
+    q_buf = [None, None]            # unit whose Q tile t is in shared memory
     s_buf = [None, None]            # (unit, block) of the S product in tile t's S columns
     s_read = [None, None]           # last (unit, block) the softmax read from them
     p_buf = [None, None]            # (unit, block) of the P stored for tile t
@@ -80,8 +82,9 @@ def simulate(units, decoupled, stages, mutate=None, seed=0):
                 continue
             for t in range(2):
                 uq = sum(1 for v in units[:u] if v[0] > 0)
-                if uq > 0:
+                if uq > 0 and mutate != "load_skips_q_empty":
                     yield ("q_empty", t), (uq - 1) & 1
+                q_buf[t] = u
                 bar(("q_full", t)).arrive()
             for j in range(J):
                 for kv in range(2):
@@ -116,6 +119,8 @@ def simulate(units, decoupled, stages, mutate=None, seed=0):
                         parity ^= 1
                     if mutate != "mma_skips_s_free":
                         yield ("s_free", t), parity
+            if q_buf[t] != u:
+                raise Violation(f"S of tile {t} unit {u} reads Q of unit {q_buf[t]}")
             if s_buf[t] is not None and s_read[t] != s_buf[t]:
                 raise Violation(f"S of tile {t} overwritten before the softmax read {s_buf[t]}")
             if not decoupled and s_buf[t] is not None and s_buf[t] not in pv_done[t]:
@@ -269,6 +274,8 @@ def test_protocol_completes_and_is_safe(decoupled, stages):
     ("softmax_skips_p_free", True),
     ("load_skips_empty_wait", True),
     ("load_skips_empty_wait", False),
+    ("load_skips_q_empty", False),
+    ("load_skips_q_empty", True),
 ])
 def test_protocol_mutations_are_caught(mutation, decoupled):
     """Each mutation must end in a safety violation or a role that never
