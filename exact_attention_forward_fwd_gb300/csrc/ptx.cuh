@@ -119,14 +119,6 @@ __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
-// L2 prefetch of one box of a 3-D tensor map (no shared-memory destination and
-// no completion to wait for; the later tensor load of the box hits L2).
-__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, int y, int z) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global [%0, {%1, %2, %3}];"
-               :: "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z)
-               : "memory");
-}
-
 // Tiled bulk store of one box from shared memory to global (3-D map); it joins
 // the issuing thread's current bulk group (close it with bulk_commit).  Boxes
 // that reach past the tensor's extents are clipped.
