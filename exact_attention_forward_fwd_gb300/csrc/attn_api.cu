@@ -369,7 +369,7 @@ int attn_fp8_prep(const void* x, void* x8, float* block_scale, const signed char
     return ATTN_ERR_ALIGNMENT;
   int sms = 0;
   if ((rc = device_check(&sms))) return rc;
-  cudaError_t e = launch_fp8_prep(x, x8, block_scale, signs, B * H, H, N, transpose_out,
+  cudaError_t e = launch_fp8_prep(x, x8, block_scale, signs, B * H, H, N, transpose_out, sms,
                                   reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
@@ -407,9 +407,10 @@ int attn_fwd_fp8(const void* q8, const void* k8, const void* v8t, const float* q
 int attn_device_status(int clear) {
   if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_ERR_CUDA;
   int out = ATTN_OK;
-  const int s[4] = {status_attn_bf16_d64(clear != 0), status_attn_bf16_d128(clear != 0),
-                    status_attn_fp8_d128(clear != 0), status_attn_bwd(clear != 0)};
-  for (int i = 0; i < 4; ++i)
+  const int s[5] = {status_attn_bf16_d64(clear != 0), status_attn_bf16_d128(clear != 0),
+                    status_attn_fp8_d128(clear != 0), status_attn_bwd(clear != 0),
+                    status_fp8_prep(clear != 0)};
+  for (int i = 0; i < 5; ++i)
     if (s[i] != 0 && out == ATTN_OK) out = s[i];
   return out;
 }

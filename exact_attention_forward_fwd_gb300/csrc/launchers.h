@@ -19,9 +19,11 @@ int status_attn_bf16_d128(bool clear);
 int status_attn_fp8_d128(bool clear);
 
 // FP8 operand preparation: x bf16 [BH][N][128] -> e4m3 (row layout, or
-// transposed [BH][128][Npad]) plus per-128-row-block scales.
+// transposed [BH][128][Npad]) plus per-128-row-block scales; persistent grid of
+// two CTAs per SM (sms = the device's SM count).
 cudaError_t launch_fp8_prep(const void* x, void* x8, float* scales, const signed char* signs,
-                            int BH, int H, int N, int transpose_out, cudaStream_t stream);
+                            int BH, int H, int N, int transpose_out, int sms, cudaStream_t stream);
+int status_fp8_prep(bool clear);
 
 // Split-KV merge of `splits` partial results ([splits][BH][N][D] fp32 O,
 // [splits][BH][N] lse) into O bf16 [BH][N][D] and lse [BH][N] (lse may be null).

@@ -67,17 +67,23 @@ def test_prep_without_rotation_is_exact(N, transpose):
         assert not pad.any()
 
 
+@pytest.mark.parametrize("transpose", [False, True])
 @pytest.mark.parametrize("N", [128, 300, 1024])
-def test_prep_with_rotation(N):
+def test_prep_with_rotation(N, transpose):
     """Q/K path: rotation computed in f32 by the kernel, in f64 by the oracle.
     Scales agree to f32 rounding; codes agree exactly except where the exact
     value lies within the f32 transform error bound of a rounding boundary,
-    where the neighbouring code is also accepted (those cases are counted)."""
+    where the neighbouring code is also accepted (those cases are counted).
+    The transposed output (any operand may ask for it) holds the same codes,
+    and zeros in its padding."""
     B, H = 2, 3
     x, _, _ = inputs.make_qkv(B, H, N, 128, seed=N + 5, outlier_frac=0.001)
     signs = inputs.make_signs(H, 128, seed=N)
-    codes, sc = ga.fp8_prep(x.cuda(), signs.cuda())
-    codes, sc = codes.cpu().numpy(), sc.cpu().numpy().astype(np.float64)
+    codes, sc = ga.fp8_prep(x.cuda(), signs.cuda(), transpose=transpose)
+    codes, pad = _rows_view(codes.cpu().numpy(), N, transpose)
+    sc = sc.cpu().numpy().astype(np.float64)
+    if pad is not None:
+        assert not pad.any()
     xf = f64(x)
     xr = ofp8.rotate(xf, signs.numpy())
     s_ref = ofp8.block_scales(xr)
