@@ -20,7 +20,7 @@ int status_attn_fp8_d128(bool clear);
 
 // FP8 operand preparation: x bf16 [BH][N][128] -> e4m3 (row layout, or
 // transposed [BH][128][Npad]) plus per-128-row-block scales; persistent grid of
-// two CTAs per SM (sms = the device's SM count).
+// three CTAs per SM (sms = the device's SM count).
 cudaError_t launch_fp8_prep(const void* x, void* x8, float* scales, const signed char* signs,
                             int BH, int H, int N, int transpose_out, int sms, cudaStream_t stream);
 int status_fp8_prep(bool clear);
