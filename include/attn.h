@@ -190,7 +190,11 @@ ATTN_API int attn_splitkv_default_splits(int B, int H, int N, int d, int causal,
  *            s = amax / 448 over the (rotated) block, or 1 if the block is all
  *            zero; codes are RNE-satfinite E4M3 of x / s (f32 division).
  *   d : 128.
- * Errors: as attn_fwd (ATTN_ERR_ALIGNMENT: x, x8 not 16-byte aligned). */
+ * The kernel loads its tiles with bounded waits, like the attention kernels: a
+ * copy that never completes sets the status word attn_device_status() reads,
+ * and the outputs are then undefined.
+ * Errors: as attn_fwd (ATTN_ERR_ALIGNMENT: x, x8 not 16-byte aligned, or signs
+ * not 4-byte aligned). */
 ATTN_API int attn_fp8_prep(const void* x, void* x8, float* block_scale, const signed char* signs, int B,
                   int H, int N, int d, int transpose_out, attn_stream_t stream);
 
