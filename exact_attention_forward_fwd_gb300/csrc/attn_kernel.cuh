@@ -704,7 +704,10 @@ __global__ void __launch_bounds__(384, 1)
             ks_nx = __ldg(ksc + j + 1);
             vs_nx = __ldg(vsc + j + 1);
           }
-          inv_vfold = __frcp_rn(v_fold);
+          // The reciprocal only scales the block's sum of p into l: the
+          // approximate instruction (within 1 ulp, subnormals kept) is enough,
+          // and measured 2.6 % faster than the correctly rounded one.
+          asm("rcp.approx.f32 %0, %1;" : "=f"(inv_vfold) : "f"(v_fold));
           lg_vfold = __log2f(v_fold);
         }
         ok = mbar_test_wait(bar(ctl.s_full[t]), sit & 1) || wait_bounded(bar(ctl.s_full[t]), sit & 1, wc);
