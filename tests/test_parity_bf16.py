@@ -84,6 +84,18 @@ def test_workload_sampled_rows(name):
     assert_bf16_parity(m, name)
 
 
+@pytest.mark.parametrize("N,d,causal", [(131149, 64, True), (65541, 128, False)])
+def test_long_sequence_sampled_rows(N, d, causal):
+    """Sequences well past the benchmark's (2^17 + 77 and 2^16 + 5 tokens, ragged
+    last tile): row, tile and key-block indices, the TMA coordinates and the
+    causal schedule at that size, on rows sampled around every tile boundary."""
+    q, k, v = inputs.make_qkv(1, 1, N, d, seed=N % 1000)
+    rows = inputs.sample_rows(N, 32, N)
+    m = _run(q, k, v, causal, rows=rows)
+    print(f"N={N} d={d} causal={causal} ({len(rows)} rows): {m}")
+    assert_bf16_parity(m, f"N={N} d={d} causal={causal}")
+
+
 def test_deterministic_and_lse_optional():
     q, k, v = (t.cuda() for t in inputs.make_qkv(2, 4, 1000, 128, seed=9))
     o1, l1 = ga.attn_fwd(q, k, v, causal=True)

@@ -10,7 +10,7 @@ from exact_attention_forward_fwd_gb300 import inputs
 from oracle import attention as oa
 from oracle import e4m3
 from oracle import fp8 as ofp8
-from parity_util import assert_fp8_fidelity, assert_fp8_parity, f64, metrics
+from parity_util import FP8_REL_RMSE, assert_fp8_fidelity, assert_fp8_parity, f64, metrics
 
 pytestmark = pytest.mark.gpu
 U = 2.0 ** -24
@@ -232,6 +232,24 @@ def test_fp8_attention_workload_sampled_rows():
     print(f"fp8 workload ({len(rows)} rows): vs exact {m}; vs quantised operands {mq}")
     assert_fp8_parity(m, w.name)
     assert_fp8_fidelity(mq, w.name)
+
+
+def test_fp8_attention_long_sequence_sampled_rows():
+    """FP8 on 2^16 + 5 tokens (prep and attention; ragged last block of the
+    block scales and of V's transposed padding), rows sampled around every
+    tile boundary.  The kernel's own error is gated against the oracle run on
+    the same E4M3 operands (the second FP8 check), and the error against the
+    exact result by its relative size.  The absolute RMSE gate of the FP8
+    workload is not applied: on this input the E4M3 operands themselves (the
+    method, with its 0.1 % outliers) put the exact result 0.029 away, which the
+    kernel-only check separates out."""
+    N = 65541
+    rows = inputs.sample_rows(N, 32, 5)
+    m, mq = _fp8_run((1, 1, N, False, 5), rows=rows)
+    print(f"fp8 N={N} ({len(rows)} rows): vs exact {m}; vs quantised operands {mq}")
+    assert m["finite"], "non-finite output"
+    assert m["rel_rmse"] <= FP8_REL_RMSE, f"relative rmse {m['rel_rmse']:.3e}"
+    assert_fp8_fidelity(mq, f"N={N}")
 
 
 def test_fp8_writes_stay_inside_outputs():

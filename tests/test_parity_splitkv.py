@@ -95,6 +95,22 @@ def test_workload_sampled_rows_default_splits(name):
     assert_bf16_parity(m, name)
 
 
+def test_long_sequence_splits():
+    """One head of 2^17 + 77 tokens (causal, d = 64) in 8 key ranges: ranges of
+    up to 16k keys per unit, the merge over them, and the ragged last tile, on
+    rows sampled around every tile boundary.  (The library's default split
+    count here is 1: the head alone has 513 units.)"""
+    N = 131149
+    q, k, v = inputs.make_qkv(1, 1, N, 64, seed=41)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert ga.splitkv_default_splits(1, 1, N, 64, True, sms) == 1
+    splits = 8
+    rows = inputs.sample_rows(N, 32, 41)
+    m = _run(q, k, v, True, splits, rows=rows)
+    print("N=131149 splits", splits, m)
+    assert_bf16_parity(m, f"N={N} splits={splits}")
+
+
 def test_workspace_contents_do_not_matter_and_repeatable():
     q, k, v = [t.cuda() for t in inputs.make_qkv(1, 2, 1000, 128, seed=3)]
     need = ga.splitkv_workspace_bytes(1, 2, 1000, 128, 5)
