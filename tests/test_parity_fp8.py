@@ -49,7 +49,7 @@ def test_e4m3_conversion_over_all_bf16_values():
 
 
 @pytest.mark.parametrize("transpose", [False, True])
-@pytest.mark.parametrize("N", [128, 300, 1024])
+@pytest.mark.parametrize("N", [1, 77, 128, 300, 1024])
 def test_prep_without_rotation_is_exact(N, transpose):
     """V path: codes decided in f32 (x / s, s = amax / 448) on both sides."""
     x, _, _ = inputs.make_qkv(2, 3, N, 128, seed=N + 3, outlier_frac=0.001)
@@ -68,7 +68,7 @@ def test_prep_without_rotation_is_exact(N, transpose):
 
 
 @pytest.mark.parametrize("transpose", [False, True])
-@pytest.mark.parametrize("N", [128, 300, 1024])
+@pytest.mark.parametrize("N", [1, 77, 128, 300, 1024])
 def test_prep_with_rotation(N, transpose):
     """Q/K path: rotation computed in f32 by the kernel, in f64 by the oracle.
     Scales agree to f32 rounding; codes agree exactly except where the exact
