@@ -114,7 +114,23 @@ struct KCfg {
   static constexpr int kTileBytes = 128 * kRowBytes;       // 128-row tile (V / V^T tile the same)
   static constexpr int kStages = (kTileBytes == 32768) ? 4 : 8;
   static constexpr int kOStageBytes = D == 128 ? 16384 : 0;   // per tile: 4 warps x 32 rows x 64 bf16 of O
-  static constexpr int kSmemBytes = (2 + kStages) * kTileBytes + 2 * kOStageBytes + 1024;
+  // bf16 at d = 64: the normaliser l~ (the sum of P as rounded to bf16) comes
+  // from the tensor core instead of two bf16 additions per key pair in the
+  // softmax.  P.V runs with N = D + 16: B is the V tile and, one operand atom
+  // along N further (the descriptor's 16 KB leading-dimension step), a block
+  // of bf16 ones, so columns [D, D + 16) of the tile's accumulator collect
+  // sum_k P[r][k] -- every one of them l~ -- in the same instructions as O.
+  static constexpr bool kLFused = !FP8 && D == 64;
+  static constexpr int kOCols = kLFused ? D + 16 : D;     // TMEM columns of O_t (and l~)
+  // Ring: K tiles take the even slots and V tiles the odd ones (items
+  // alternate K, V and every unit starts on an even item); with kLFused each
+  // V slot is followed by its 16 KB of ones.
+  static constexpr int kPairBytes = (kLFused ? 3 : 2) * kTileBytes;
+  static constexpr int kRingBytes = kStages / 2 * kPairBytes;
+  __host__ __device__ static constexpr uint32_t slot_off(uint32_t s) {
+    return kLFused ? (s >> 1) * kPairBytes + (s & 1) * kTileBytes : s * kTileBytes;
+  }
+  static constexpr int kSmemBytes = 2 * kTileBytes + kRingBytes + 2 * kOStageBytes + 1024;
   static constexpr uint32_t kTmemCols = 512;
   // 12 warps: two softmax warpgroups (warps 0-7), then load (8), MMA (9) and
   // two idle warps (10, 11) that complete the third warpgroup so that it can
@@ -137,24 +153,30 @@ struct KCfg {
   // memory, so a tile's next S product can start as soon as its softmax has
   // read S, and P.V reads P as an SS operand.
   static constexpr bool kPSmem = FP8;
-  // bf16 at d = 64: P has TMEM columns of its own (the 128 that d = 64 leaves
-  // free: tile t at [256 + 2D + 64 t, +64)), so S_t(j+1) need not wait for
-  // P_t(j).V either.  Both forms take the decoupled issue order below.
+  // bf16 at d = 64: P of keys [0, 96) has TMEM columns of its own (tile t at
+  // [kPCol + 48 t, +48): the 96 columns left after S, O and l~), and P of
+  // keys [96, 128) goes over S's last 16 columns.  S is issued in two parts:
+  // keys [0, 112) as soon as the softmax has read the tile's previous S, and
+  // keys [112, 128) right after the P.V steps that read P's last keys, so
+  // S_t(j+1) waits for a sixth of P_t(j).V instead of all of it.
   static constexpr bool kPSep = !FP8 && D == 64;
-  static constexpr bool kDecoupled = kPSmem || kPSep;
+  static constexpr int kSMainKeys = 112;                  // keys of S's first part
+  static constexpr bool kDecoupled = kPSmem;
   // Tile t's P-ready barrier is p_ready[t * kPReadyStride].  Neither the
   // spacing nor the spare word between the bf16 barriers carries a signal;
   // both are what measured fastest (same-box A/B, three repeats): FP8 1.6 %
   // faster with its two barriers adjacent, bf16 d = 128 1 % faster with them
   // 16 bytes apart and the word between them initialised as a barrier too.
   static constexpr int kPReadyStride = FP8 ? 1 : 2;
-  static constexpr uint32_t kPCol = 256 + 2 * D;
+  static constexpr uint32_t kPCol = 256 + 2 * kOCols;
   static constexpr int kSKSteps = FP8 ? D / 32 : D / 16;  // k-steps of S = Q K^T
   static constexpr int kPVSteps = FP8 ? 4 : 8;            // k-steps of O += P V (128 keys)
   static constexpr uint32_t kIdescS =
       make_idesc(128, 128, FP8 ? 0u : 1u, FP8 ? 0u : 1u, false, false);
   static constexpr uint32_t kIdescPV =
-      make_idesc(128, D, FP8 ? 0u : 1u, FP8 ? 0u : 1u, false, !FP8);
+      make_idesc(128, kOCols, FP8 ? 0u : 1u, FP8 ? 0u : 1u, false, !FP8);
+  static constexpr uint32_t kIdescSMain = make_idesc(128, kSMainKeys, 1u, 1u, false, false);
+  static constexpr uint32_t kIdescSTail = make_idesc(128, 128 - kSMainKeys, 1u, 1u, false, false);
 };
 
 struct SmemCtl {
@@ -276,7 +298,7 @@ __global__ void __launch_bounds__(384, 1)
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sQ = smem_addr(smem);                         // Q tile 0, Q tile 1
   const uint32_t sKV = sQ + 2 * C::kTileBytes;                 // ring of K / V tiles
-  const uint32_t sO = sKV + C::kStages * C::kTileBytes;        // O staging (d = 128), 4 KB per softmax warp
+  const uint32_t sO = sKV + C::kRingBytes;                     // O staging (d = 128), 4 KB per softmax warp
                                                                // (FP8: also P, 128 bytes per row)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -308,6 +330,17 @@ __global__ void __launch_bounds__(384, 1)
     ctl.abort_flag = 0;
     fence_mbarrier_init();
     fence_proxy_async_smem();
+  }
+  if constexpr (C::kLFused) {
+    // The ones beside each V slot (bf16 1.0 = 0x3F80 in every element: with
+    // equal elements the swizzle needs no care), written once.
+    constexpr int kChunks = C::kStages / 2 * C::kTileBytes / 16;
+    for (int i = threadIdx.x; i < kChunks; i += C::kThreads) {
+      const int pr = i / (C::kTileBytes / 16), c = i % (C::kTileBytes / 16);
+      st_shared_v4(sKV + C::slot_off(2 * pr + 1) + C::kTileBytes + 16 * c, 0x3F803F80u, 0x3F803F80u,
+                   0x3F803F80u, 0x3F803F80u);
+    }
+    fence_proxy_async_smem();   // generic-proxy writes -> the MMA's operand reads
   }
   if (warp == 9) {
     tmem_alloc(smem_addr(&ctl.tmem_base), C::kTmemCols);
@@ -398,7 +431,7 @@ __global__ void __launch_bounds__(384, 1)
             const uint32_t ph = (item / C::kStages) & 1;
             ok = wait_bounded(bar(ctl.kv_empty[slot]), ph ^ 1, wc);
             if (!ok) break;
-            const uint32_t dst = sKV + slot * C::kTileBytes;
+            const uint32_t dst = sKV + C::slot_off(slot);
             mbar_arrive_expect_tx(bar(ctl.kv_full[slot]), C::kTileBytes);
             if (kv == 0) {
               for (int s = 0; s < C::kSlabs; ++s)
@@ -447,7 +480,7 @@ __global__ void __launch_bounds__(384, 1)
       const uint32_t idesc_s = C::kIdescS | (p.neg_scale ? kIdescNegateB : 0u);
       auto s_mma = [&](int t, uint32_t kslot) {
         const uint64_t da = dQ + t * kTileUnits;
-        const uint64_t db = dK + kslot * kTileUnits;
+        const uint64_t db = dK + (C::slot_off(kslot) >> 4);
 #pragma unroll
         for (int g = 0; g < C::kSKSteps / 4; ++g) {
           const uint64_t o = FP8 ? 0 : g * 1024;   // next 128-byte column slab (bf16, d = 128)
@@ -458,11 +491,11 @@ __global__ void __launch_bounds__(384, 1)
       // bf16 with P over S (d = 128): O_t += P_t V over the keys of half `hf` of
       // the block, P from the tile's S columns.
       auto pv_mma = [&](int t, uint32_t vslot, bool acc, int hf) {
-        const uint64_t db = dV + vslot * kTileUnits;
+        const uint64_t db = dV + (C::slot_off(vslot) >> 4);
         const uint32_t ta = tmem + 128 * t;
         const uint32_t acc0 = (acc || hf > 0) ? 1u : 0u;
         const int k = 4 * hf;   // 16-key steps: P columns advance by 8, V rows by 2048 bytes
-        mma_ts_x4_w<false>(tmem + 256 + D * t, ta + k * 8, ta + k * 8 + 8, ta + k * 8 + 16,
+        mma_ts_x4_w<false>(tmem + 256 + C::kOCols * t, ta + k * 8, ta + k * 8 + 8, ta + k * 8 + 16,
                            ta + k * 8 + 24, db + k * 128, db + k * 128 + 128, db + k * 128 + 256,
                            db + k * 128 + 384, C::kIdescPV, acc0);
       };
@@ -488,29 +521,15 @@ __global__ void __launch_bounds__(384, 1)
           mma_commit_w(bar(ctl.s_full[t]));
           return true;
         };
-        // O_t (+)= P_t V over the block's 128 keys once P_t is stored: FP8,
-        // four K = 32 steps with P from shared memory; bf16, eight K = 16
-        // steps with P from its TMEM columns (16 keys = 8 columns per step,
-        // V rows 2048 bytes apart).
+        // O_t (+)= P_t V over the block's 128 keys once P_t is stored: four
+        // K = 32 steps with P from shared memory.
         auto issue_pv = [&](int t, uint32_t vslot, bool acc) -> bool {
-          const uint64_t db = dV + vslot * kTileUnits;
+          const uint64_t db = dV + (C::slot_off(vslot) >> 4);
           if (!wait_w(ctl.p_ready[t * C::kPReadyStride], npv & 1)) return false;
           tc_fence_after();
-          if constexpr (FP8) {
-            const uint64_t da = dP + t * (uint64_t)(C::kOStageBytes >> 4);
-            mma_ss_x4_w<true>(tmem + 256 + D * t, da, da + 2, da + 4, da + 6, db, db + 2, db + 4,
-                              db + 6, C::kIdescPV, acc ? 1u : 0u);
-          } else {
-            const uint32_t ta = tmem + C::kPCol + 64 * t;
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-              const int k = 4 * hf;
-              mma_ts_x4_w<false>(tmem + 256 + D * t, ta + k * 8, ta + k * 8 + 8, ta + k * 8 + 16,
-                                 ta + k * 8 + 24, db + k * 128, db + k * 128 + 128,
-                                 db + k * 128 + 256, db + k * 128 + 384, C::kIdescPV,
-                                 (acc || hf > 0) ? 1u : 0u);
-            }
-          }
+          const uint64_t da = dP + t * (uint64_t)(C::kOStageBytes >> 4);
+          mma_ss_x4_w<true>(tmem + 256 + D * t, da, da + 2, da + 4, da + 6, db, db + 2, db + 4,
+                            db + 6, C::kIdescPV, acc ? 1u : 0u);
           mma_commit_w(bar(ctl.p_free[t]));
           return true;
         };
@@ -547,6 +566,96 @@ __global__ void __launch_bounds__(384, 1)
             if (!(ok = issue_pv(1, iv % C::kStages, j > 0))) break;
             mma_commit_w(bar(ctl.kv_empty[iv % C::kStages]));
             if (j == J - 1) mma_commit_w(bar(ctl.o_final[1]));
+            ++npv;
+          }
+          ++uit;
+        }
+      } else if constexpr (C::kPSep) {
+        // bf16 d = 64 (P outside S but for its last 32 keys).  Per tile and
+        // block: S(j+1) for keys [0, 112) once the softmax has read S(j)
+        // (s_free) and K(j+1) has landed; once P(j) is stored (p_ready), the
+        // P.V steps over keys [96, 128) -- P from S's last 16 columns --,
+        // then S(j+1) for keys [112, 128) over those columns and s_full, then
+        // the P.V steps over keys [0, 96) and p_free.
+        uint32_t ns[2] = {0, 0};   // S products issued per tile
+        uint32_t npv = 0;          // P.V products issued per tile
+        const uint32_t idesc_main = C::kIdescSMain | (p.neg_scale ? kIdescNegateB : 0u);
+        const uint32_t idesc_tail = C::kIdescSTail | (p.neg_scale ? kIdescNegateB : 0u);
+        auto s_main = [&](int t, uint32_t kslot) -> bool {
+          if (ns[t] > 0 && !wait_w(ctl.s_free[t], (ns[t] - 1) & 1)) return false;
+          ++ns[t];
+          tc_fence_after();
+          const uint64_t da = dQ + t * kTileUnits;
+          const uint64_t db = dK + (C::slot_off(kslot) >> 4);
+          mma_ss_x4_w<false>(tmem + 128 * t, da, da + 2, da + 4, da + 6, db, db + 2, db + 4, db + 6,
+                             idesc_main, 0u);
+          return true;
+        };
+        auto s_tail = [&](int t, uint32_t kslot) {
+          const uint64_t da = dQ + t * kTileUnits;
+          const uint64_t db = dK + ((C::slot_off(kslot) + C::kSMainKeys * 128) >> 4);
+          mma_ss_x4_w<false>(tmem + 128 * t + C::kSMainKeys, da, da + 2, da + 4, da + 6, db, db + 2,
+                             db + 4, db + 6, idesc_tail, 0u);
+          mma_commit_w(bar(ctl.s_full[t]));
+        };
+        // P.V over 16-key step k: P from the tile's own columns (k < 6) or
+        // from S's last 16 columns (k = 6, 7); V rows 2048 bytes apart.
+        auto pa = [&](int t, int k) -> uint32_t {
+          return k < 6 ? tmem + C::kPCol + 48 * t + 8 * k : tmem + 128 * t + C::kSMainKeys + 8 * (k - 6);
+        };
+        for (uint32_t k = 0; ok; ++k) {
+          Unit w{};
+          if (!take_unit(k, ok, w)) break;
+          const int J = w.nblocks;
+          if (J == 0) continue;
+          ok = wait_w(ctl.q_full[0], uit & 1) && wait_w(ctl.q_full[1], uit & 1);
+          if (!ok) break;
+          const uint32_t base = item;   // K_j = base + 2j, V_j = base + 2j + 1
+          item += 2 * J;
+          if (!(ok = wait_item(base))) break;
+          // The previous unit's last P.V steps (already issued) read P's last
+          // keys before these products overwrite them.
+          if (!(ok = s_main(0, base % C::kStages))) break;
+          s_tail(0, base % C::kStages);
+          if (!(ok = s_main(1, base % C::kStages))) break;
+          s_tail(1, base % C::kStages);
+          mma_commit_w(bar(ctl.kv_empty[base % C::kStages]));
+          if (J == 1) {
+            mma_commit_w(bar(ctl.q_empty[0]));
+            mma_commit_w(bar(ctl.q_empty[1]));
+          }
+          for (int j = 0; j < J && ok; ++j) {
+            const uint32_t iv = base + 2 * j + 1, ik = base + 2 * j + 2;
+            const uint32_t vslot = iv % C::kStages, kslot = ik % C::kStages;
+            const bool nxt = j + 1 < J;
+            if (nxt) {
+              if (!(ok = wait_item(ik))) break;
+              if (!(ok = s_main(0, kslot) && s_main(1, kslot))) break;
+            }
+            if (!(ok = wait_item(iv))) break;
+            const uint64_t db = dV + (C::slot_off(vslot) >> 4);
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              if (!(ok = wait_w(ctl.p_ready[t * C::kPReadyStride], npv & 1))) break;
+              tc_fence_after();
+              const uint32_t dO = tmem + 256 + C::kOCols * t;
+              mma_ts_x2_w(dO, pa(t, 6), pa(t, 7), db + 6 * 128, db + 7 * 128, C::kIdescPV, j > 0 ? 1u : 0u);
+              if (nxt) s_tail(t, kslot);
+              mma_ts_x4_w<false>(dO, pa(t, 0), pa(t, 1), pa(t, 2), pa(t, 3), db, db + 128, db + 256,
+                                 db + 384, C::kIdescPV, 1u);
+              mma_ts_x2_w(dO, pa(t, 4), pa(t, 5), db + 4 * 128, db + 5 * 128, C::kIdescPV, 1u);
+              mma_commit_w(bar(ctl.p_free[t]));
+              if (j == J - 1) mma_commit_w(bar(ctl.o_final[t]));
+            }
+            if (!ok) break;
+            mma_commit_w(bar(ctl.kv_empty[vslot]));
+            if (nxt) {
+              mma_commit_w(bar(ctl.kv_empty[kslot]));
+              if (j + 2 == J) {
+                mma_commit_w(bar(ctl.q_empty[0]));
+                mma_commit_w(bar(ctl.q_empty[1]));
+              }
+            }
             ++npv;
           }
           ++uit;
@@ -627,9 +736,11 @@ __global__ void __launch_bounds__(384, 1)
     const int r = wq * 32 + lane;            // row within the tile
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + lane_off + 128 * t;
-    const uint32_t tO = tmem + lane_off + 256 + D * t;
-    // bf16 P: over S (d = 128), or in its own columns (d = 64).
-    const uint32_t tP = C::kPSep ? tmem + lane_off + C::kPCol + 64 * t : tS;
+    const uint32_t tO = tmem + lane_off + 256 + C::kOCols * t;
+    // bf16 P: over S (d = 128), or in its own columns but for its last 32
+    // keys, which go over S's last 16 columns (d = 64).
+    const uint32_t tP = C::kPSep ? tmem + lane_off + C::kPCol + 48 * t : tS;
+    const uint32_t tL = tO + D;   // bf16 d = 64: l~ of this row (16 equal columns)
     const float NEG_INF = __int_as_float(0xff800000);
     const bool zero_scale = p.zero_scale != 0;
     uint32_t sit = 0, uit = 0;
@@ -767,6 +878,15 @@ __global__ void __launch_bounds__(384, 1)
             for (int i = 0; i < 32; ++i) orow[i] = __float_as_uint(__uint_as_float(orow[i]) * alpha);
             tmem_st32(tO + cc, orow);
           }
+          if constexpr (C::kLFused) {
+            uint32_t lrow[16];
+            tmem_ld16(tL, lrow);
+            tmem_wait_ld();
+            reg_fence(lrow);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) lrow[i] = __float_as_uint(__uint_as_float(lrow[i]) * alpha);
+            tmem_st16(tL, lrow);
+          }
         };
         if constexpr (FP8) {
           // p' = p * v_fold = 2^(s c - (m - log2 v_fold)) against the running
@@ -886,12 +1006,16 @@ __global__ void __launch_bounds__(384, 1)
               pk[i] = pb;
               const uint64_t e = f32x2_pack(p0, p1);
               if (ii & 1) {
-                r2 = add_bf16_lo(pb, r2);
-                r3 = add_bf16_hi(pb, r3);
+                if constexpr (!C::kLFused) {
+                  r2 = add_bf16_lo(pb, r2);
+                  r3 = add_bf16_hi(pb, r3);
+                }
                 ex1 = f32x2_add(ex1, e);
               } else {
-                r0 = add_bf16_lo(pb, r0);
-                r1 = add_bf16_hi(pb, r1);
+                if constexpr (!C::kLFused) {
+                  r0 = add_bf16_lo(pb, r0);
+                  r1 = add_bf16_hi(pb, r1);
+                }
                 ex0 = f32x2_add(ex0, e);
               }
             }
@@ -948,7 +1072,12 @@ __global__ void __launch_bounds__(384, 1)
             tmem_st32(tP, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
           }
           __syncwarp();   // tcgen05.st is warp-collective
-          tmem_st32(tP + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+          if constexpr (C::kPSep) {
+            tmem_st16(tP + 32, *reinterpret_cast<uint32_t(*)[16]>(&pk[32]));
+            tmem_st16(tS + C::kSMainKeys, *reinterpret_cast<uint32_t(*)[16]>(&pk[48]));
+          } else {
+            tmem_st32(tP + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+          }
           // bf16: one signal for all keys of the block (P·V waits for it once).
           tmem_wait_st();
           tc_fence_before();
@@ -967,8 +1096,17 @@ __global__ void __launch_bounds__(384, 1)
       float inv;
       if (FP8)
         inv = (ell > 0.0f) ? v_smax / C::kPScale / ell : 0.0f;
-      else
+      else {
+        if constexpr (C::kLFused) {
+          // l~ as the tensor core summed the block products' P (all 16 columns equal).
+          uint32_t lrow[16];
+          tmem_ld16(tL, lrow);
+          tmem_wait_ld();
+          reg_fence(lrow);
+          ell_r = __uint_as_float(lrow[0]);
+        }
         inv = (ell_r > 0.0f) ? 1.0f / ell_r : 0.0f;
+      }
       const bool live = row < p.N;
       const float l2e = (ell > 0.0f) ? (m_ref + __log2f(ell)) * 0.69314718055994531f : NEG_INF;
       if (p.o_part != nullptr) {

@@ -492,6 +492,16 @@ __device__ __forceinline__ void mma_ts_x4_w(uint32_t d_tmem, uint32_t a0, uint32
   }
 }
 
+__device__ __forceinline__ void mma_ts_x2_w(uint32_t d_tmem, uint32_t a0, uint32_t a1, uint64_t b0,
+                                            uint64_t b1, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q, e;\n\tsetp.ne.b32 p, %6, 0;\n\tsetp.eq.b32 q, %5, %5;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1." GB300_MMA_KIND_F16 " [%0], [%1], %3, %5, p;\n\t"
+      "@e tcgen05.mma.cta_group::1." GB300_MMA_KIND_F16 " [%0], [%2], %4, %5, q;\n\t}\n" ::"r"(d_tmem),
+      "r"(a0), "r"(a1), "l"(b0), "l"(b1), "r"(idesc), "r"(accumulate));
+}
+
 __device__ __forceinline__ void mma_commit_w(uint32_t bar) {
   asm volatile(
       "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
