@@ -1051,6 +1051,20 @@ __global__ void __launch_bounds__(384, 1)
           __syncwarp();   // tcgen05.st is warp-collective
           tmem_st32(tP, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
           exps_half(x, 1, es1, rs1);
+          // P of keys [64, 128).  At d = 64 it is stored before the block's sum
+          // is tested (a retaken block stores both halves again before P is
+          // signalled): measured 0.6 % faster there, but 4 % slower at d = 128,
+          // which stores it after the test.
+          auto store_p_hi = [&]() {
+            __syncwarp();   // tcgen05.st is warp-collective
+            if constexpr (C::kPSep) {
+              tmem_st16(tP + 32, *reinterpret_cast<uint32_t(*)[16]>(&pk[32]));
+              tmem_st16(tS + C::kSMainKeys, *reinterpret_cast<uint32_t(*)[16]>(&pk[48]));
+            } else {
+              tmem_st32(tP + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+            }
+          };
+          if constexpr (C::kPSep) store_p_hi();
           e_sum = es0 + es1;
           r_sum = rs0 + rs1;
           // A sum of 128 terms above 2^32 has a term above 2^25; moving m to the
@@ -1068,16 +1082,12 @@ __global__ void __launch_bounds__(384, 1)
             exps_half(x, 1, es1, rs1);
             e_sum = es0 + es1;
             r_sum = rs0 + rs1;
+            tmem_wait_st();   // this block's first stores are done before they are replaced
             __syncwarp();
             tmem_st32(tP, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+            if constexpr (C::kPSep) store_p_hi();
           }
-          __syncwarp();   // tcgen05.st is warp-collective
-          if constexpr (C::kPSep) {
-            tmem_st16(tP + 32, *reinterpret_cast<uint32_t(*)[16]>(&pk[32]));
-            tmem_st16(tS + C::kSMainKeys, *reinterpret_cast<uint32_t(*)[16]>(&pk[48]));
-          } else {
-            tmem_st32(tP + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
-          }
+          if constexpr (!C::kPSep) store_p_hi();
           // bf16: one signal for all keys of the block (P·V waits for it once).
           tmem_wait_st();
           tc_fence_before();
