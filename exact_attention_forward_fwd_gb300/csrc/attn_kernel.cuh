@@ -155,10 +155,11 @@ struct KCfg {
   static constexpr bool kPSmem = FP8;
   // bf16 at d = 64: P of keys [0, 96) has TMEM columns of its own (tile t at
   // [kPCol + 48 t, +48): the 96 columns left after S, O and l~), and P of
-  // keys [96, 128) goes over S's last 16 columns.  S is issued in two parts:
-  // keys [0, 112) as soon as the softmax has read the tile's previous S, and
-  // keys [112, 128) right after the P.V steps that read P's last keys, so
-  // S_t(j+1) waits for a sixth of P_t(j).V instead of all of it.
+  // keys [96, 128) goes over S's last 16 columns.  The softmax computes and
+  // signals those last keys first (p_ready[2 t + 1]); S is issued in two
+  // parts: keys [0, 112) as soon as the softmax has read the tile's previous
+  // S, and keys [112, 128) right after the P.V steps that read P's last keys,
+  // so S_t(j+1) is complete while the softmax still works on block j.
   static constexpr bool kPSep = !FP8 && D == 64;
   static constexpr int kSMainKeys = 112;                  // keys of S's first part
   static constexpr bool kDecoupled = kPSmem;
@@ -197,6 +198,7 @@ struct SmemCtl {
   int4 unit_ring[4][2];     // decoded work units (Unit fields; valid = 0 ends)
   uint32_t tmem_base;
   int abort_flag;
+  uint64_t pt_done[2];      // bf16 d = 64: the tile's P.V over its last 32 keys is done
 };
 
 // Status word of launches that pass no status pointer (one per translation
@@ -323,6 +325,8 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(bar(ctl.p_free[t]), 1);
     }
     mbar_init(bar(ctl.drain), 1);
+    if constexpr (C::kPSep)
+      for (int t = 0; t < 2; ++t) mbar_init(bar(ctl.pt_done[t]), 1);
     for (int s = 0; s < 4; ++s) {
       mbar_init(bar(ctl.unit_full[s]), 1);
       mbar_init(bar(ctl.unit_empty[s]), 9);   // the MMA warp and the 8 softmax warps
@@ -571,12 +575,14 @@ __global__ void __launch_bounds__(384, 1)
           ++uit;
         }
       } else if constexpr (C::kPSep) {
-        // bf16 d = 64 (P outside S but for its last 32 keys).  Per tile and
-        // block: S(j+1) for keys [0, 112) once the softmax has read S(j)
-        // (s_free) and K(j+1) has landed; once P(j) is stored (p_ready), the
-        // P.V steps over keys [96, 128) -- P from S's last 16 columns --,
-        // then S(j+1) for keys [112, 128) over those columns and s_full, then
-        // the P.V steps over keys [0, 96) and p_free.
+        // bf16 d = 64 (P outside S but for its last 32 keys).  Per block:
+        // S(j+1) for keys [0, 112) of each tile once its softmax has read S(j)
+        // (s_free) and K(j+1) has landed; then, for each tile once P(j) of
+        // keys [96, 128) is stored (p_ready[2 t + 1]), the P.V steps over those
+        // keys -- P from S's last 16 columns -- with a commit to pt_done, and
+        // S(j+1) for keys [112, 128) over those columns with s_full; then, for
+        // each tile once the rest of P(j) is stored (p_ready[2 t]), the P.V
+        // steps over keys [0, 96) and p_free.
         uint32_t ns[2] = {0, 0};   // S products issued per tile
         uint32_t npv = 0;          // P.V products issued per tile
         const uint32_t idesc_main = C::kIdescSMain | (p.neg_scale ? kIdescNegateB : 0u);
@@ -636,11 +642,19 @@ __global__ void __launch_bounds__(384, 1)
             const uint64_t db = dV + (C::slot_off(vslot) >> 4);
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
+              if (!(ok = wait_w(ctl.p_ready[t * C::kPReadyStride + 1], npv & 1))) break;
+              tc_fence_after();
+              mma_ts_x2_w(tmem + 256 + C::kOCols * t, pa(t, 6), pa(t, 7), db + 6 * 128, db + 7 * 128,
+                          C::kIdescPV, j > 0 ? 1u : 0u);
+              mma_commit_w(bar(ctl.pt_done[t]));
+              if (nxt) s_tail(t, kslot);
+            }
+            if (!ok) break;
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
               if (!(ok = wait_w(ctl.p_ready[t * C::kPReadyStride], npv & 1))) break;
               tc_fence_after();
               const uint32_t dO = tmem + 256 + C::kOCols * t;
-              mma_ts_x2_w(dO, pa(t, 6), pa(t, 7), db + 6 * 128, db + 7 * 128, C::kIdescPV, j > 0 ? 1u : 0u);
-              if (nxt) s_tail(t, kslot);
               mma_ts_x4_w<false>(dO, pa(t, 0), pa(t, 1), pa(t, 2), pa(t, 3), db, db + 128, db + 256,
                                  db + 384, C::kIdescPV, 1u);
               mma_ts_x2_w(dO, pa(t, 4), pa(t, 5), db + 4 * 128, db + 5 * 128, C::kIdescPV, 1u);
@@ -974,6 +988,100 @@ __global__ void __launch_bounds__(384, 1)
             if (!ok) break;
           }
           ell += e_sum;
+        } else if constexpr (C::kPSep) {
+          // bf16, d = 64.  p = 2^(s*c - m) against the running reference m, as
+          // at d = 128 below (the block's sum bounds every p; a block whose sum
+          // passes 2^32 moves m to its max and is taken again), with two
+          // differences: l~ comes from the tensor core (the ones beside V), and
+          // P of keys [96, 128) is computed, tested, stored over S's last 16
+          // columns and signalled first, so that the tile's P.V over those keys
+          // and the rest of its next S run while the softmax works on keys
+          // [0, 96).  If the whole block's sum then fails the test, O and l~
+          // already hold P.V over the last keys at the old reference: once that
+          // product is done (pt_done) they are rescaled with the rest, and the
+          // sum of those keys' p is scaled by the same factor.
+          uint32_t pk[64];
+          // Exponentials of key pairs [i0, i0 + n) into pk[i0, i0 + n); returns
+          // their sum of p.
+          auto exps_pairs = [&](const float (&x)[128], int i0, int n) -> float {
+            const float m_use = (m_ref == NEG_INF) ? 0.0f : m_ref;
+            const uint64_t c2 = f32x2_pack(cj, cj);
+            const uint64_t nm2 = f32x2_pack(-m_use, -m_use);
+            uint64_t ex0 = 0, ex1 = 0;   // (0.f, 0.f)
+#pragma unroll
+            for (int ii = 0; ii < n; ++ii) {
+              const int i = i0 + ii;
+              float t0, t1;
+              f32x2_unpack(f32x2_fma(f32x2_pack(x[2 * i], x[2 * i + 1]), c2, nm2), t0, t1);
+              const float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
+              pk[i] = pack_bf16x2(p0, p1);
+              if (ii & 1)
+                ex1 = f32x2_add(ex1, f32x2_pack(p0, p1));
+              else
+                ex0 = f32x2_add(ex0, f32x2_pack(p0, p1));
+            }
+            float b0, b1;
+            f32x2_unpack(f32x2_add(ex0, ex1), b0, b1);
+            return b0 + b1;
+          };
+          // Rows with `redo` move m to the block's max; returns their factor.
+          auto move_ref = [&](const float (&x)[128], bool redo) -> float {
+            const float m_blk = row_max(x) * cj;
+            const float m_new = redo ? fmaxf(m_ref, m_blk) : m_ref;
+            const float alpha = redo ? ex2_approx(m_ref - m_new) : 1.0f;   // 0 when m_ref = -inf
+            ell *= alpha;
+            m_ref = m_new;
+            return alpha;
+          };
+          float x[128];
+          load_s(x);
+          // S is in registers now: the tile's next S product may overwrite it.
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(ctl.s_free[t]));
+          if (!__all_sync(0xffffffffu, m_ref != NEG_INF)) {
+            const float m_blk0 = row_max(x) * cj;
+            if (m_ref == NEG_INF) m_ref = m_blk0;
+          }
+          float sum_tail = exps_pairs(x, 48, 16);
+          if (__any_sync(0xffffffffu, !(sum_tail <= C::kSumLimit))) {
+            const float alpha = move_ref(x, !(sum_tail <= C::kSumLimit));
+            if (jj > 0) {
+              if (!(ok = wait_pfree())) break;
+              rescale_o(alpha);
+            }
+            sum_tail = exps_pairs(x, 48, 16);
+          }
+          __syncwarp();   // tcgen05.st is warp-collective
+          tmem_st16(tS + C::kSMainKeys, *reinterpret_cast<uint32_t(*)[16]>(&pk[48]));
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(bar(ctl.p_ready[t * C::kPReadyStride + 1]));
+          float sum_main = exps_pairs(x, 0, 32);
+          if (!(ok = wait_pfree())) break;
+          __syncwarp();
+          tmem_st32(tP, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+          sum_main += exps_pairs(x, 32, 16);
+          __syncwarp();
+          tmem_st16(tP + 32, *reinterpret_cast<uint32_t(*)[16]>(&pk[32]));
+          if (__any_sync(0xffffffffu, !(sum_tail + sum_main <= C::kSumLimit))) {
+            const uint32_t pb = bar(ctl.pt_done[t]), ph = np & 1;
+            if (!(ok = __all_sync(0xffffffffu, mbar_test_wait(pb, ph) || wait_bounded(pb, ph, wc)))) break;
+            tc_fence_after();
+            const float alpha = move_ref(x, !(sum_tail + sum_main <= C::kSumLimit));
+            rescale_o(alpha);
+            sum_tail *= alpha;
+            sum_main = exps_pairs(x, 0, 32) + exps_pairs(x, 32, 16);
+            tmem_wait_st();   // this block's first stores are done before they are replaced
+            __syncwarp();
+            tmem_st32(tP, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+            tmem_st16(tP + 32, *reinterpret_cast<uint32_t(*)[16]>(&pk[32]));
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(bar(ctl.p_ready[t * C::kPReadyStride]));
+          ++np;
+          ell += sum_tail + sum_main;
         } else {
           // p = 2^(s*c - m) against the running reference max m, so no
           // exponential waits for the block's max.  The block's sum of p bounds
@@ -1006,16 +1114,12 @@ __global__ void __launch_bounds__(384, 1)
               pk[i] = pb;
               const uint64_t e = f32x2_pack(p0, p1);
               if (ii & 1) {
-                if constexpr (!C::kLFused) {
-                  r2 = add_bf16_lo(pb, r2);
-                  r3 = add_bf16_hi(pb, r3);
-                }
+                r2 = add_bf16_lo(pb, r2);
+                r3 = add_bf16_hi(pb, r3);
                 ex1 = f32x2_add(ex1, e);
               } else {
-                if constexpr (!C::kLFused) {
-                  r0 = add_bf16_lo(pb, r0);
-                  r1 = add_bf16_hi(pb, r1);
-                }
+                r0 = add_bf16_lo(pb, r0);
+                r1 = add_bf16_hi(pb, r1);
                 ex0 = f32x2_add(ex0, e);
               }
             }
@@ -1033,38 +1137,15 @@ __global__ void __launch_bounds__(384, 1)
           // nothing is rescaled.
           float x[128];
           load_s(x);
-          if constexpr (C::kPSep) {
-            // S is in registers now: the tile's next S product may overwrite it.
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(ctl.s_free[t]));
-          }
           if (!__all_sync(0xffffffffu, m_ref != NEG_INF)) {
             const float m_blk0 = row_max(x) * cj;
             if (m_ref == NEG_INF) m_ref = m_blk0;
           }
           float es0, rs0, es1, rs1;
           exps_half(x, 0, es0, rs0);
-          if constexpr (C::kPSep) {
-            if (!(ok = wait_pfree())) break;
-          }
           __syncwarp();   // tcgen05.st is warp-collective
           tmem_st32(tP, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
           exps_half(x, 1, es1, rs1);
-          // P of keys [64, 128).  At d = 64 it is stored before the block's sum
-          // is tested (a retaken block stores both halves again before P is
-          // signalled): measured 0.6 % faster there, but 4 % slower at d = 128,
-          // which stores it after the test.
-          auto store_p_hi = [&]() {
-            __syncwarp();   // tcgen05.st is warp-collective
-            if constexpr (C::kPSep) {
-              tmem_st16(tP + 32, *reinterpret_cast<uint32_t(*)[16]>(&pk[32]));
-              tmem_st16(tS + C::kSMainKeys, *reinterpret_cast<uint32_t(*)[16]>(&pk[48]));
-            } else {
-              tmem_st32(tP + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
-            }
-          };
-          if constexpr (C::kPSep) store_p_hi();
           e_sum = es0 + es1;
           r_sum = rs0 + rs1;
           // A sum of 128 terms above 2^32 has a term above 2^25; moving m to the
@@ -1085,14 +1166,15 @@ __global__ void __launch_bounds__(384, 1)
             tmem_wait_st();   // this block's first stores are done before they are replaced
             __syncwarp();
             tmem_st32(tP, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-            if constexpr (C::kPSep) store_p_hi();
           }
-          if constexpr (!C::kPSep) store_p_hi();
+          // P of keys [64, 128), after the sum test (storing it before the test
+          // measured 4 % slower here).
+          __syncwarp();   // tcgen05.st is warp-collective
+          tmem_st32(tP + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
           // bf16: one signal for all keys of the block (P·V waits for it once).
           tmem_wait_st();
           tc_fence_before();
           mbar_arrive(bar(ctl.p_ready[t * C::kPReadyStride]));
-          if constexpr (C::kPSep) ++np;
           ell_r += r_sum;
           ell += e_sum;
         }

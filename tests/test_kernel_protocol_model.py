@@ -13,8 +13,13 @@ for both issue orders the kernel uses:
     P buffer only after the previous P.V completed (p_free);
   * split (bf16, d = 64): as decoupled, but P's last keys are stored over the
     tail columns of S, so S_t(j+1) is issued in two parts -- its main part
-    after s_free, its tail only after the P.V steps that read P's last keys
-    (and before the remaining P.V steps, with s_full).
+    after s_free, its tail only after the P.V steps that read P's last keys.
+    The softmax stores and signals those last keys first (p_tail), the MMA
+    warp then issues their P.V steps (commit: pt_done) and S's tail (s_full),
+    and the rest of P follows (p_ready: the remaining P.V steps, p_free).  A
+    retaken block rescales O: before signalling the last keys after waiting
+    for the previous block's P.V (p_free), or after it once their P.V is done
+    (pt_done).
 Units are random sequences of key-block counts (split-KV's empty ranges
 included).  Completions (TMA copies, tcgen05 commits) arrive as soon as they
 are issued, which only removes delays and so cannot hide a deadlock.
@@ -25,8 +30,9 @@ P.V reads the P it is meant to, and no P is overwritten before its P.V read
 it; the K/V ring never refills a slot before its tile was consumed; every
 product of a unit is issued before the unit's output is read; no S product
 reads a Q tile the next unit's copy has replaced; in the split order, no S
-tail overwrites P's last keys before their P.V steps read them, and the
-softmax reads an S whose two parts are both of the block.  Mutations of the
+tail overwrites P's last keys before their P.V steps read them, the softmax
+reads an S whose two parts are both of the block, and O is rescaled only
+while no product accumulates into it.  Mutations of the
 protocol (a wait dropped, a wrong parity, a barrier shared by two P buffers,
 an S tail issued too early) must be caught.
 """
@@ -306,7 +312,8 @@ def simulate_split(units, stages, mutate=None, seed=0):
     for s in range(stages):
         bar(("kv_full", s)), bar(("kv_empty", s))
     for t in range(2):
-        for n in ("q_full", "q_empty", "s_full", "p_ready", "o_final", "s_free", "p_free"):
+        for n in ("q_full", "q_empty", "s_full", "p_ready", "p_tail", "pt_done", "o_final",
+                  "s_free", "p_free"):
             bar((n, t))
     ring = [None] * stages
     q_buf = [None, None]
@@ -316,8 +323,10 @@ def simulate_split(units, stages, mutate=None, seed=0):
     p_main = [None, None]       # P in the tile's own columns
     p_main_used = [None, None]
     p_tail_used = [None, None]  # last (unit, block) whose P.V read P's last keys
-    pv_done = [set(), set()]
+    pv_done = [set(), set()]    # (unit, block) whose P.V main steps ran
+    tail_done = [set(), set()]  # (unit, block) whose P.V steps over the last keys ran
     pipe = deque()
+    redo_rng = random.Random(seed + 7)
     mma_done = [False]
 
     def load():
@@ -369,6 +378,7 @@ def simulate_split(units, stages, mutate=None, seed=0):
         if s_tail_buf[t] != ("P", u, j):
             raise Violation(f"P.V of tile {t} block {(u, j)} reads P's last keys of {s_tail_buf[t]}")
         p_tail_used[t] = (u, j)
+        tail_done[t].add((u, j))
 
     def run_pv_main(u, t, j, vitem):
         if ring[vitem % stages] != vitem:
@@ -433,12 +443,15 @@ def simulate_split(units, stages, mutate=None, seed=0):
                     yield from s_main(u, 1, j + 1, ik)
                 yield ("kv_full", iv % stages), (iv // stages) & 1
                 for t in range(2):
-                    yield ("p_ready", t), npv & 1
+                    yield ("p_tail", t), npv & 1
                     if mutate == "mma_tail_before_pv" and nxt:
                         s_tail(u, t, j + 1, ik)
                     issue(run_pv_tail, u, t, j, iv)
+                    commit(("pt_done", t))
                     if nxt and mutate != "mma_tail_before_pv":
                         s_tail(u, t, j + 1, ik)
+                for t in range(2):
+                    yield ("p_ready", t), npv & 1
                     issue(run_pv_main, u, t, j, iv)
                     commit(("p_free", t))
                     if j == J - 1:
@@ -452,8 +465,17 @@ def simulate_split(units, stages, mutate=None, seed=0):
             uit += 1
         mma_done[0] = True
 
+    def rescale(t, u, j, done):
+        """O_t is rescaled: every P.V step that accumulates into it so far must
+        have run (`done` lists the steps issued before this point)."""
+        for kind, key in done:
+            if key not in (tail_done[t] if kind == "tail" else pv_done[t]):
+                raise Violation(f"O of tile {t} rescaled at {(u, j)} while P.V {kind} {key} "
+                                f"has not run")
+
     def softmax(t):
         sit, np_, uit = 0, 0, 0
+        prev = None
         for u, (J, _) in enumerate(units):
             if J == 0:
                 continue
@@ -465,14 +487,31 @@ def simulate_split(units, stages, mutate=None, seed=0):
                                     f"{s_main_buf[t]} / {s_tail_buf[t]}")
                 s_read[t] = (u, j)
                 bar(("s_free", t)).arrive()
-                if np_ > 0 and mutate != "softmax_skips_p_free":
+                pfree_seen = np_ == 0
+                # A retake found on the last keys: wait for the previous P.V,
+                # then rescale (O holds the unit's earlier blocks only).
+                if j > 0 and redo_rng.random() < 0.15:
+                    if not pfree_seen and mutate != "softmax_skips_p_free":
+                        yield ("p_free", t), (np_ - 1) & 1
+                        pfree_seen = True
+                    rescale(t, u, j, [("main", prev)])
+                s_tail_buf[t] = ("P", u, j)   # P's last keys over S's tail (already read)
+                bar(("p_tail", t)).arrive()
+                if not pfree_seen and mutate != "softmax_skips_p_free":
                     yield ("p_free", t), (np_ - 1) & 1
                 if p_main[t] is not None and p_main_used[t] != p_main[t]:
                     raise Violation(f"P of tile {t} block {p_main[t]} overwritten before its P.V")
                 p_main[t] = (u, j)
-                s_tail_buf[t] = ("P", u, j)   # P's last keys over S's tail (already read)
+                # A retake found on the whole block: O already takes P.V over
+                # this block's last keys; wait for it (pt_done), then rescale.
+                if redo_rng.random() < 0.15:
+                    if mutate != "softmax_skips_pt_done":
+                        yield ("pt_done", t), np_ & 1
+                    steps = [("tail", (u, j))] + ([("main", prev)] if j > 0 else [])
+                    rescale(t, u, j, steps)
                 bar(("p_ready", t)).arrive()
                 np_ += 1
+                prev = (u, j)
             yield ("o_final", t), uit & 1
             missing = [j for j in range(J) if (u, j) not in pv_done[t]]
             if missing:
@@ -514,6 +553,7 @@ def test_protocol_completes_and_is_safe(decoupled, stages, split):
     ("mma_skips_s_free", True, True),
     ("softmax_skips_p_free", True, True),
     ("mma_tail_before_pv", True, True),
+    ("softmax_skips_pt_done", True, True),
 ])
 def test_protocol_mutations_are_caught(mutation, decoupled, split):
     """Each mutation must end in a safety violation or a role that never
