@@ -169,6 +169,56 @@ def test_one_dominant_key(d, causal, scale):
     assert np.abs(f64(o) - vv).max() <= 2 ** -8 * np.abs(vv).max()
 
 
+def _retake_scores(head, N=512):
+    """Scores (natural log units, scale 1) of every row for head `head`:
+    uniform in [0, 1) but for key block 2 (keys 256-383):
+      0: its last 32 keys at 19 and key 296 at 24.  The last keys alone pass
+         the 2^32 bound on a block's sum of p; the whole block does not, so
+         the reference moves by about 33 (base 2) after those keys were
+         weighed, and they keep about 18 % of the block's weight;
+      1: its last 32 keys at 24 (they alone fail the bound);
+      2: keys 296 and 356 at 12 (a rise of about 17: no retake).
+    The values are bf16-exact."""
+    g = torch.Generator().manual_seed(900 + head)
+    s = torch.rand(N, generator=g)
+    if head == 0:
+        s[352:384] = 19.0
+        s[296] = 24.0
+    elif head == 1:
+        s[352:384] = 24.0
+    else:
+        s[296] = 12.0
+        s[356] = 12.0
+    return s.to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_retake_with_weighty_earlier_keys(d, causal):
+    """A block whose sum of p fails the 2^32 bound moves the reference to its
+    max and is taken again, and what O and the sums already hold is rescaled.
+    At d = 64 the kernel weighs a block's last 32 keys first and issues their
+    P.V before testing the rest, so in head 0 those keys' product is already
+    in O when the block fails; unlike the one-dominant-key case, the rescaled
+    keys here keep a share of the row's weight (about 18 %) far above the
+    gates, so a product rescaled wrongly, or rescaled before it landed, shows.
+    Head 1 fails on its last keys alone, head 2 only moves the reference
+    lazily.  Q is e_0 for every row and K's first column carries the scores."""
+    N, H = 512, 3
+    q = torch.zeros(1, H, N, d, dtype=torch.bfloat16)
+    q[..., 0] = 1.0
+    k = torch.zeros(1, H, N, d, dtype=torch.bfloat16)
+    for h in range(H):
+        k[0, h, :, 0] = _retake_scores(h, N)
+    _, _, v = inputs.make_qkv(1, H, N, d, seed=950 + d)
+    o, lse, m = _bf16(q, k, v, causal, 1.0)
+    assert_bf16_parity(m, f"retake d={d} causal={causal}")
+    if not causal:
+        # Head 0, every row: the rescaled last keys of block 2 weigh about 18 %.
+        w = torch.softmax(_retake_scores(0, N).double(), 0)
+        assert 0.15 < float(w[352:384].sum()) < 0.21
+
+
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
 def test_constant_v(d, causal):
