@@ -22,6 +22,7 @@ from exact_attention_forward_fwd_gb300 import inputs
 from oracle import attention as oa
 from parity_util import (assert_bf16_parity, assert_fp8_fidelity, assert_fp8_parity, f64,
                          metrics)
+from retake_cases import retake_scores
 
 pytestmark = pytest.mark.gpu
 
@@ -169,29 +170,6 @@ def test_one_dominant_key(d, causal, scale):
     assert np.abs(f64(o) - vv).max() <= 2 ** -8 * np.abs(vv).max()
 
 
-def _retake_scores(head, N=512):
-    """Scores (natural log units, scale 1) of every row for head `head`:
-    uniform in [0, 1) but for key block 2 (keys 256-383):
-      0: its last 32 keys at 19 and key 296 at 24.  The last keys alone pass
-         the 2^32 bound on a block's sum of p; the whole block does not, so
-         the reference moves by about 33 (base 2) after those keys were
-         weighed, and they keep about 18 % of the block's weight;
-      1: its last 32 keys at 24 (they alone fail the bound);
-      2: keys 296 and 356 at 12 (a rise of about 17: no retake).
-    The values are bf16-exact."""
-    g = torch.Generator().manual_seed(900 + head)
-    s = torch.rand(N, generator=g)
-    if head == 0:
-        s[352:384] = 19.0
-        s[296] = 24.0
-    elif head == 1:
-        s[352:384] = 24.0
-    else:
-        s[296] = 12.0
-        s[356] = 12.0
-    return s.to(torch.bfloat16)
-
-
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
 def test_retake_with_weighty_earlier_keys(d, causal):
@@ -209,13 +187,13 @@ def test_retake_with_weighty_earlier_keys(d, causal):
     q[..., 0] = 1.0
     k = torch.zeros(1, H, N, d, dtype=torch.bfloat16)
     for h in range(H):
-        k[0, h, :, 0] = _retake_scores(h, N)
+        k[0, h, :, 0] = retake_scores(h, N)
     _, _, v = inputs.make_qkv(1, H, N, d, seed=950 + d)
     o, lse, m = _bf16(q, k, v, causal, 1.0)
     assert_bf16_parity(m, f"retake d={d} causal={causal}")
     if not causal:
         # Head 0, every row: the rescaled last keys of block 2 weigh about 18 %.
-        w = torch.softmax(_retake_scores(0, N).double(), 0)
+        w = torch.softmax(retake_scores(0, N).double(), 0)
         assert 0.15 < float(w[352:384].sum()) < 0.21
 
 
