@@ -25,11 +25,17 @@
 //   * warp 9: allocates TMEM and issues every tcgen05.mma (the warp runs its
 //     loop converged, one elected lane issues):
 //       S_t = Q_t K_j^T  (SS, both operands K-major in shared memory)
-//       O_t += P_t V_j   (TS, P from TMEM, V from shared memory)
-//     ordered PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), ... so the tensor pipe
-//     always has the other tile's work while one tile's softmax runs;
+//       O_t += P_t V_j   (TS, P from TMEM, V from shared memory; FP8: SS)
+//     bf16 at d = 128 in the order PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), ...
+//     (P over S: the tensor pipe has the other tile's work while one tile's
+//     softmax runs); FP8 issues S_t(j+1) as soon as the softmax has read
+//     S_t(j) (P in shared memory); bf16 at d = 64 does the same for S's
+//     first 112 keys and issues the rest once the P.V steps over P's last
+//     32 keys, stored over S's last 16 columns and signalled first, are in;
 //   * TMEM columns: S/P tile 0 [0,128), S/P tile 1 [128,256), O tile 0
-//     [256,256+D), O tile 1 [256+D, 256+2D);
+//     [256,256+D), O tile 1 [256+D, 256+2D); at d = 64 O_t has 80 columns
+//     (the last 16 accumulate l~: P.V runs with N = 80 against V and a block
+//     of ones) and P of keys [0, 96) has [416 + 48 t, +48);
 //   * scale folded into exp2: p = 2^(s * scale*log2(e) - m), m kept in the
 //     same base-2 units; a negative scale runs as s' = Q (-K)^T with |scale|
 //     (the MMA negates its B operand, exactly), so the multiplier the softmax
@@ -48,8 +54,11 @@
 //     reference only when that max exceeds it by more than 8, so p <= 2^8
 //     (P must fit E4M3, whose largest value is 448).
 //   * because every tcgen05.commit tracks all earlier MMAs of the issuing
-//     thread, the arrival of S_t(j) also proves O_t += P_t(j-1) V(j-1) is
-//     complete: a rescale of O~ right after waiting for S_t(j) is race-free.
+//     thread, in the d = 128 order the arrival of S_t(j) also proves
+//     O_t += P_t(j-1) V(j-1) is complete: a rescale of O~ right after waiting
+//     for S_t(j) is race-free.  The other orders wait for the commit after
+//     the previous P.V (p_free) and, at d = 64 once P's last keys are in,
+//     for the commit after their P.V steps (pt_done).
 //
 // FP8 variant (E4M3 operands, f32 accumulation): per-128-row block scales of
 // Q, K, V ("FlashAttention-3: How Warp Specialization ...", section 4); the
@@ -145,8 +154,9 @@ struct KCfg {
   static constexpr float kTauLog2 = 8.0f;                 // FP8: move the reference when a block max exceeds it by more
   static constexpr float kPScale = 1.75f;                 // FP8: P' = p * kPScale * s_V(j) / max s_V <= 256 * 1.75 = 448
   // Causal: tile 0 skips a pair's last key block (wholly above its rows).  bf16
-  // at d = 128 only: the FP8 and d = 64 kernels measured 2 % slower with the
-  // extra branches in their issue loop than the work saved.
+  // at d = 128 only: the FP8 and d = 64 kernels measured slower with the
+  // extra branches in their issue loop than the work saved (2 %; at d = 64,
+  // in the coupled order with the l~ product, 1.3 %).
   static constexpr bool kSkipDiag = !FP8 && D == 128;
   // FP8: P (one byte per key, 128 bytes per row) goes to shared memory -- the
   // region that stages O in the epilogue -- instead of over S in tensor
@@ -186,10 +196,11 @@ struct SmemCtl {
   uint64_t q_full[2];
   uint64_t q_empty[2];
   uint64_t s_full[2];
-  uint64_t p_ready[4];      // tile t at [t * kPReadyStride]
-  uint64_t s_free[2];       // decoupled order (FP8, d = 64): the tile's S has been read (its
-                            // TMEM columns may be overwritten)
-  uint64_t p_free[2];       // decoupled order: the tile's P.V is done (its P buffer may be
+  uint64_t p_ready[4];      // tile t at [t * kPReadyStride]; d = 64: P's last 32 keys at
+                            // [t * kPReadyStride + 1]
+  uint64_t s_free[2];       // FP8, d = 64: the tile's S has been read (its TMEM columns
+                            // may be overwritten)
+  uint64_t p_free[2];       // FP8, d = 64: the tile's P.V is done (its P buffer may be
                             // overwritten, O_t rescaled)
   uint64_t o_final[2];
   uint64_t drain;
@@ -507,10 +518,9 @@ __global__ void __launch_bounds__(384, 1)
         return wait_w(ctl.kv_full[it % C::kStages], (it / C::kStages) & 1);
       };
       if constexpr (C::kDecoupled) {
-        // P outside the S columns (FP8: shared memory; bf16 d = 64: TMEM
-        // columns of its own).  S_t(j+1) is issued once the softmax has read
-        // S_t(j) (s_free) and K_{j+1} has landed; P_t(j).V_j once P_t(j) is
-        // stored.  A tile's softmax therefore never waits for its own
+        // FP8: P outside the S columns, in shared memory.  S_t(j+1) is issued
+        // once the softmax has read S_t(j) (s_free) and K_{j+1} has landed;
+        // P_t(j).V_j once P_t(j) is stored.  A tile's softmax therefore never waits for its own
         // products: the next S is computed while it works on the current
         // block.  p_free (a commit after each P.V) tells the softmax that the
         // P buffer may be refilled and O rescaled.
