@@ -54,11 +54,12 @@ def test_more_units_than_sms(causal):
     assert_bf16_parity(_run(q, k, v, causal), "16x16x300", rounding_floor=causal)
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("scale", [1.0, 0.01, 0.3])
-def test_other_scales(scale):
-    q, k, v = inputs.make_qkv(1, 2, 384, 128, seed=5)
-    # scale 1: scores of spread ~11, rows nearly one-hot, O of unit size.
-    assert_bf16_parity(_run(q, k, v, True, scale=scale), f"scale={scale}", rounding_floor=True)
+def test_other_scales(scale, d):
+    q, k, v = inputs.make_qkv(1, 2, 384, d, seed=5)
+    # scale 1: scores of spread ~11 (d = 128), rows nearly one-hot, O of unit size.
+    assert_bf16_parity(_run(q, k, v, True, scale=scale), f"scale={scale} d={d}", rounding_floor=True)
 
 
 @pytest.mark.parametrize("name", ["n256_d64", "n2048_d128", "n2048_d128_causal", "n2048_d128_k8",
@@ -96,8 +97,9 @@ def test_long_sequence_sampled_rows(N, d, causal):
     assert_bf16_parity(m, f"N={N} d={d} causal={causal}")
 
 
-def test_deterministic_and_lse_optional():
-    q, k, v = (t.cuda() for t in inputs.make_qkv(2, 4, 1000, 128, seed=9))
+@pytest.mark.parametrize("d", [64, 128])
+def test_deterministic_and_lse_optional(d):
+    q, k, v = (t.cuda() for t in inputs.make_qkv(2, 4, 1000, d, seed=9))
     o1, l1 = ga.attn_fwd(q, k, v, causal=True)
     o2, l2 = ga.attn_fwd(q, k, v, causal=True)
     o3, l3 = ga.attn_fwd(q, k, v, causal=True, return_lse=False)
