@@ -520,10 +520,10 @@ __global__ void __launch_bounds__(384, 1)
       if constexpr (C::kDecoupled) {
         // FP8: P outside the S columns, in shared memory.  S_t(j+1) is issued
         // once the softmax has read S_t(j) (s_free) and K_{j+1} has landed;
-        // P_t(j).V_j once P_t(j) is stored.  A tile's softmax therefore never waits for its own
-        // products: the next S is computed while it works on the current
-        // block.  p_free (a commit after each P.V) tells the softmax that the
-        // P buffer may be refilled and O rescaled.
+        // P_t(j).V_j once P_t(j) is stored.  A tile's softmax therefore never
+        // waits for its own products: the next S is computed while it works
+        // on the current block.  p_free (a commit after each P.V) tells the
+        // softmax that the P buffer may be refilled and O rescaled.
         uint32_t ns[2] = {0, 0};   // S products issued per tile
         uint32_t npv = 0;          // P.V products issued per tile
         const uint64_t dP = make_smem_desc(sO, 16, 1024, kSwizzle128B);
