@@ -1054,6 +1054,10 @@ __global__ void __launch_bounds__(384, 1)
             if (m_ref == NEG_INF) m_ref = m_blk0;
           }
           float sum_tail = exps_pairs(x, 48, 16);
+          // Stored before its sum is tested (a retake stores it again before
+          // the signal): 0.5 % faster than storing after the test.
+          __syncwarp();   // tcgen05.st is warp-collective
+          tmem_st16(tS + C::kSMainKeys, *reinterpret_cast<uint32_t(*)[16]>(&pk[48]));
           if (__any_sync(0xffffffffu, !(sum_tail <= C::kSumLimit))) {
             const float alpha = move_ref(x, !(sum_tail <= C::kSumLimit));
             if (jj > 0) {
@@ -1061,9 +1065,10 @@ __global__ void __launch_bounds__(384, 1)
               rescale_o(alpha);
             }
             sum_tail = exps_pairs(x, 48, 16);
+            tmem_wait_st();
+            __syncwarp();
+            tmem_st16(tS + C::kSMainKeys, *reinterpret_cast<uint32_t(*)[16]>(&pk[48]));
           }
-          __syncwarp();   // tcgen05.st is warp-collective
-          tmem_st16(tS + C::kSMainKeys, *reinterpret_cast<uint32_t(*)[16]>(&pk[48]));
           tmem_wait_st();
           tc_fence_before();
           mbar_arrive(bar(ctl.p_ready[t * C::kPReadyStride + 1]));
