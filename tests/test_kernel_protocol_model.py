@@ -5,7 +5,7 @@ producer/consumer pipeline", checks a warp-specialised pipeline by modelling
 its producer and consumers.  This file models the forward kernel's own roles
 -- the load warp, the MMA-issuing warp and the two query tiles' softmax warps
 -- with every mbarrier wait and arrival in the order the kernel performs them,
-for both issue orders the kernel uses:
+for the three issue orders the kernel uses:
   * coupled (bf16, d = 128): P is written over S in TMEM, so S_t(j+1) is issued
     after P_t(j).V; causal units may let tile 0 skip the pair's last block;
   * decoupled (FP8: P in shared memory): S_t(j+1) is issued once the softmax
@@ -16,29 +16,35 @@ for both issue orders the kernel uses:
     after s_free, its tail only after the P.V steps that read P's last keys.
     The softmax stores and signals those last keys first (p_tail), the MMA
     warp then issues their P.V steps (commit: pt_done) and S's tail (s_full),
-    and the rest of P follows (p_ready: the remaining P.V steps, p_free).  A
-    retaken block rescales O: before signalling the last keys after waiting
-    for the previous block's P.V (p_free), or after it once their P.V is done
-    (pt_done).
+    and the rest of P follows (p_ready: the remaining P.V steps, p_free).
+The MMA warp's products and commits go into an in-order tensor pipe that a
+role of its own executes at any later point: a product reads and writes its
+buffers when it runs, and a commit arrives once everything issued before it
+has run.  Copies land as soon as they are issued, which only removes delays.
+Every role runs at a random speed, so that one can run far ahead of another.
+Softmax blocks are retaken at random (the reference moves and O is rescaled):
+the coupled order rescales right after the block's S arrived, the decoupled
+order after the previous P.V (p_free), the split order before signalling P's
+last keys (after p_free) or after it (after pt_done).
 Units are random sequences of key-block counts (split-KV's empty ranges
-included).  Completions (TMA copies, tcgen05 commits) arrive as soon as they
-are issued, which only removes delays and so cannot hide a deadlock.
+included).
 
-Checked: every role finishes (no wait that never completes); every S product
-lands in a TMEM buffer whose previous S the softmax has already read; every
-P.V reads the P it is meant to, and no P is overwritten before its P.V read
-it; the K/V ring never refills a slot before its tile was consumed; every
-product of a unit is issued before the unit's output is read; no S product
-reads a Q tile the next unit's copy has replaced; in the split order, no S
-tail overwrites P's last keys before their P.V steps read them, the softmax
-reads an S whose two parts are both of the block, and O is rescaled only
-while no product accumulates into it.  Mutations of the
-protocol (a wait dropped, a wrong parity, a barrier shared by two P buffers,
-an S tail issued too early) must be caught.
+Checked at every step: every role finishes (no wait that never completes); no
+S product overwrites an S the softmax has not read or a P whose P.V has not
+run; every P.V reads the P of its block; no P is refilled before its P.V
+ran; the K/V ring never refills a slot before its tile was consumed; no
+product reads a Q tile the next unit's copy has replaced; the softmax reads S
+only once all of it is the block's; O is rescaled only once every product
+accumulating into it has run, and read only once all of the unit's have.
+Mutations of the protocol (a wait dropped, a wrong parity, a product issued
+out of order, a barrier shared by two P buffers) must be caught.
 """
 import random
+from collections import deque
 
 import pytest
+
+ORDERS = ("coupled", "decoupled", "split")
 
 
 class Bar:
@@ -63,213 +69,12 @@ class Violation(Exception):
     pass
 
 
-def simulate(units, decoupled, stages, mutate=None, seed=0, split=False):
-    """Runs the roles over `units`, a list of (nblocks, skip0) per unit.
-    Returns the roles still waiting (empty when all finished); raises
-    Violation on a safety failure."""
-    if split:
-        return simulate_split(units, stages, mutate, seed)
-    bars = {}
-
-    def bar(name, count=1):
-        return bars.setdefault(name, Bar(count))
-
-    for s in range(stages):
-        bar(("kv_full", s)), bar(("kv_empty", s))
-    for t in range(2):
-        for n in ("q_full", "q_empty", "s_full", "p_ready", "o_final", "s_free", "p_free"):
-            bar((n, t))
-    # Safety state: what each TMEM / shared buffer holds.
-    ring = [None] * stages          # item index held by each ring slot
-    q_buf = [None, None]            # unit whose Q tile t is in shared memory
-    s_buf = [None, None]            # (unit, block) of the S product in tile t's S columns
-    s_read = [None, None]           # last (unit, block) the softmax read from them
-    p_buf = [None, None]            # (unit, block) of the P stored for tile t
-    p_used = [None, None]           # last (unit, block) whose P.V read that P
-    pv_done = [set(), set()]        # (unit, block) P.V issued per tile
-
-    def load():
-        item = 0
-        for u, (J, _) in enumerate(units):
-            if J == 0:
-                continue
-            for t in range(2):
-                uq = sum(1 for v in units[:u] if v[0] > 0)
-                if uq > 0 and mutate != "load_skips_q_empty":
-                    yield ("q_empty", t), (uq - 1) & 1
-                q_buf[t] = u
-                bar(("q_full", t)).arrive()
-            for j in range(J):
-                for kv in range(2):
-                    slot, ph = item % stages, (item // stages) & 1
-                    if mutate != "load_skips_empty_wait":
-                        yield ("kv_empty", slot), ph ^ 1
-                    if ring[slot] is not None:
-                        raise Violation(f"ring slot {slot} refilled while item {ring[slot]} is in use")
-                    ring[slot] = item
-                    bar(("kv_full", slot)).arrive()
-                    item += 1
-
-    def consume(item):
-        slot = item % stages
-        yield ("kv_full", slot), (item // stages) & 1
-        if ring[slot] != item:
-            raise Violation(f"item {item} not in slot {slot} (holds {ring[slot]})")
-
-    def release(item):
-        ring[item % stages] = None
-        bar(("kv_empty", item % stages)).arrive()
-
-    def mma():
-        item, uit = 0, 0
-        ns, npv = [0, 0], [0, 0]
-
-        def s_product(u, t, j):
-            if decoupled:
-                if ns[t] > 0:
-                    parity = (ns[t] - 1) & 1
-                    if mutate == "mma_s_free_wrong_parity":
-                        parity ^= 1
-                    if mutate != "mma_skips_s_free":
-                        yield ("s_free", t), parity
-            if q_buf[t] != u:
-                raise Violation(f"S of tile {t} unit {u} reads Q of unit {q_buf[t]}")
-            if s_buf[t] is not None and s_read[t] != s_buf[t]:
-                raise Violation(f"S of tile {t} overwritten before the softmax read {s_buf[t]}")
-            if not decoupled and s_buf[t] is not None and s_buf[t] not in pv_done[t]:
-                raise Violation(f"S/P columns of tile {t} overwritten before P.V of {s_buf[t]}")
-            s_buf[t] = (u, j)
-            ns[t] += 1
-            bar(("s_full", t)).arrive()
-
-        def pv_product(u, t, j):
-            parity = npv[t] & 1
-            yield ("p_ready", t), parity
-            if p_buf[t] != (u, j):
-                raise Violation(f"P.V of tile {t} block {(u, j)} reads P of {p_buf[t]}")
-            p_used[t] = (u, j)
-            pv_done[t].add((u, j))
-            npv[t] += 1
-            if decoupled:
-                bar(("p_free", t)).arrive()
-
-        for u, (J, skip0) in enumerate(units):
-            if J == 0:
-                continue
-            yield ("q_full", 0), uit & 1
-            yield ("q_full", 1), uit & 1
-            base = item
-            item += 2 * J
-            if decoupled:
-                yield from consume(base)
-                yield from s_product(u, 0, 0)
-                yield from s_product(u, 1, 0)
-                release(base)
-                if J == 1:
-                    bar(("q_empty", 0)).arrive(), bar(("q_empty", 1)).arrive()
-                for j in range(J):
-                    iv, ik = base + 2 * j + 1, base + 2 * j + 2
-                    if j + 1 < J:
-                        yield from consume(ik)
-                        yield from s_product(u, 0, j + 1)
-                        yield from s_product(u, 1, j + 1)
-                        release(ik)
-                        if j + 2 == J:
-                            bar(("q_empty", 0)).arrive(), bar(("q_empty", 1)).arrive()
-                    yield from consume(iv)
-                    yield from pv_product(u, 0, j)
-                    if j == J - 1:
-                        bar(("o_final", 0)).arrive()
-                    yield from pv_product(u, 1, j)
-                    release(iv)
-                    if j == J - 1:
-                        bar(("o_final", 1)).arrive()
-            else:
-                J0 = J - 1 if skip0 else J
-                yield from consume(base)
-                yield from s_product(u, 0, 0)
-                yield from s_product(u, 1, 0)
-                release(base)
-                if J == 1:
-                    bar(("q_empty", 0)).arrive(), bar(("q_empty", 1)).arrive()
-                for j in range(J):
-                    iv, ik = base + 2 * j + 1, base + 2 * j + 2
-                    yield from consume(iv)
-                    if j < J0:
-                        yield from pv_product(u, 0, j)
-                        if j == J0 - 1:
-                            bar(("o_final", 0)).arrive()
-                    if j + 1 < J:
-                        yield from consume(ik)
-                        if j + 1 < J0:
-                            yield from s_product(u, 0, j + 1)
-                    yield from pv_product(u, 1, j)
-                    release(iv)
-                    if j == J - 1:
-                        bar(("o_final", 1)).arrive()
-                    if j + 1 < J:
-                        yield from s_product(u, 1, j + 1)
-                        release(ik)
-                        if j + 2 == J:
-                            bar(("q_empty", 0)).arrive(), bar(("q_empty", 1)).arrive()
-            uit += 1
-
-    def softmax(t):
-        sit, np_, uit = 0, 0, 0
-        for u, (J, skip0) in enumerate(units):
-            if J == 0:
-                continue   # an empty key range: the softmax writes its empty result
-            nb = J - 1 if (skip0 and t == 0 and not decoupled) else J
-            for j in range(nb):
-                yield ("s_full", t), sit & 1
-                sit += 1
-                if s_buf[t] != (u, j):
-                    raise Violation(f"softmax {t} expected S of {(u, j)}, TMEM holds {s_buf[t]}")
-                s_read[t] = (u, j)
-                if decoupled:
-                    bar(("s_free", t)).arrive()
-                    if np_ > 0 and mutate != "softmax_skips_p_free":
-                        yield ("p_free", t), (np_ - 1) & 1
-                # P of this block replaces the tile's previous P.
-                if p_buf[t] is not None and p_used[t] != p_buf[t]:
-                    raise Violation(f"P of tile {t} block {p_buf[t]} overwritten before its P.V")
-                p_buf[t] = (u, j)
-                bar(("p_ready", t)).arrive()
-                np_ += 1
-            yield ("o_final", t), uit & 1
-            missing = [j for j in range(nb) if (u, j) not in pv_done[t]]
-            if missing:
-                raise Violation(f"tile {t} reads O of unit {u} before P.V of blocks {missing}")
-            uit += 1
-
-    roles = {"load": load(), "mma": mma(), "softmax0": softmax(0), "softmax1": softmax(1)}
-    waiting = dict.fromkeys(roles)
-    live = set(roles)
-    rng = random.Random(seed)
-    while live:
-        moved = False
-        order = sorted(live)
-        rng.shuffle(order)   # any interleaving of the roles' progress
-        for r in order:
-            w = waiting[r]
-            if w is not None and not bars[w[0]].ready(w[1]):
-                continue
-            try:
-                waiting[r] = next(roles[r])
-            except StopIteration:
-                live.discard(r)
-            moved = True
-        if not moved:
-            break
-    return {r: waiting[r] for r in live}
-
-
 def run_roles(roles, bars, seed):
     """Advances the roles in a random order until all finish or none can move.
     A role yields either (barrier, parity) or a predicate to wait on.  Each
     role gets a random speed (the chance that it takes a ready step in a
-    sweep), so that one role can run far ahead of another; the run ends when
-    no role is ready."""
+    sweep); the run ends when no role is ready.  Returns the roles still
+    waiting."""
     waiting = dict.fromkeys(roles)
     live = set(roles)
     rng = random.Random(seed)
@@ -296,14 +101,12 @@ def run_roles(roles, bars, seed):
     return {r: waiting[r] for r in live}
 
 
-def simulate_split(units, stages, mutate=None, seed=0):
-    """The split order (bf16, d = 64): S in a main part and a tail part, P's
-    last keys over the tail columns of S.  Unlike the two orders above, the
-    MMA warp's products and commits go into an in-order tensor pipe that a
-    role of its own executes at any later point, so a product reads and
-    writes its buffers when it runs and a commit arrives once everything
-    issued before it has run; the checks are made at execution."""
-    from collections import deque
+def simulate(units, order, stages, mutate=None, seed=0):
+    """Runs the roles of `order` over `units`, a list of (nblocks, skip0) per
+    unit.  Returns the roles still waiting (empty when all finished); raises
+    Violation on a safety failure."""
+    assert order in ORDERS
+    split, coupled = order == "split", order == "coupled"
     bars = {}
 
     def bar(name, count=1):
@@ -315,78 +118,73 @@ def simulate_split(units, stages, mutate=None, seed=0):
         for n in ("q_full", "q_empty", "s_full", "p_ready", "p_tail", "pt_done", "o_final",
                   "s_free", "p_free"):
             bar((n, t))
+
     ring = [None] * stages
     q_buf = [None, None]
-    s_main_buf = [None, None]   # (unit, block) of S's main columns
-    s_tail_buf = [None, None]   # (unit, block) of S's tail columns, or ("P", unit, block)
-    s_read = [None, None]
-    p_main = [None, None]       # P in the tile's own columns
-    p_main_used = [None, None]
-    p_tail_used = [None, None]  # last (unit, block) whose P.V read P's last keys
-    pv_done = [set(), set()]    # (unit, block) whose P.V main steps ran
-    tail_done = [set(), set()]  # (unit, block) whose P.V steps over the last keys ran
+    # TMEM contents of S_t's columns: "main" (coupled and decoupled: all of
+    # them) and, in the split order, "tail"; a region holds ("S", unit, block)
+    # or ("P", unit, block).
+    s_reg = [{"main": None, "tail": None}, {"main": None, "tail": None}]
+    s_read = [None, None]            # last (unit, block) whose S the softmax read
+    p_buf = [None, None]             # P outside S (FP8: shared memory; split: own columns)
+    ran = [set(), set()]             # ("tail" | "main", unit, block) P.V steps that ran
     pipe = deque()
-    redo_rng = random.Random(seed + 7)
     mma_done = [False]
+    retake_rng = random.Random(seed + 7)
 
+    # ------------------------------------------------------------ load warp
     def load():
-        item = 0
+        item, uq = 0, 0
         for u, (J, _) in enumerate(units):
             if J == 0:
                 continue
             for t in range(2):
-                uq = sum(1 for v in units[:u] if v[0] > 0)
-                if uq > 0:
+                if uq > 0 and mutate != "load_skips_q_empty":
                     yield ("q_empty", t), (uq - 1) & 1
                 q_buf[t] = u
                 bar(("q_full", t)).arrive()
+            uq += 1
             for j in range(J):
                 for kv in range(2):
                     slot, ph = item % stages, (item // stages) & 1
-                    yield ("kv_empty", slot), ph ^ 1
-                    if ring[slot] is not None:
-                        raise Violation(f"ring slot {slot} refilled while item {ring[slot]} is in use")
+                    if mutate != "load_skips_empty_wait":
+                        yield ("kv_empty", slot), ph ^ 1
+                        if ring[slot] is not None:
+                            raise Violation(f"ring slot {slot} refilled while item {ring[slot]} "
+                                            f"is in use")
                     ring[slot] = item
                     bar(("kv_full", slot)).arrive()
                     item += 1
 
-    # ------------------------------------------------ products, run by the pipe
-    def run_s_main(u, t, j, kitem):
-        if ring[kitem % stages] != kitem:
-            raise Violation(f"S of tile {t} reads ring item {ring[kitem % stages]}, not {kitem}")
+    # ---------------------------------------- products, run by the tensor pipe
+    def check_ring(item, what):
+        if ring[item % stages] != item:
+            raise Violation(f"{what} reads ring item {ring[item % stages]}, not {item}")
+
+    def run_s(t, u, j, kitem, reg):
+        check_ring(kitem, f"S of tile {t} {(u, j)}")
         if q_buf[t] != u:
             raise Violation(f"S of tile {t} unit {u} reads Q of unit {q_buf[t]}")
-        if s_main_buf[t] is not None and s_read[t] != s_main_buf[t]:
-            raise Violation(f"S of tile {t} overwritten before the softmax read {s_main_buf[t]}")
-        s_main_buf[t] = (u, j)
+        held = s_reg[t][reg]
+        if held is not None:
+            kind, key = held[0], held[1:]
+            if kind == "S" and s_read[t] != key:
+                raise Violation(f"S ({reg}) of tile {t} overwritten before the softmax read {key}")
+            if kind == "P" and ("tail" if split else "main", *key) not in ran[t]:
+                raise Violation(f"S ({reg}) of tile {t} overwrites P of {key} before its P.V")
+        s_reg[t][reg] = ("S", u, j)
 
-    def run_s_tail(u, t, j, kitem):
-        if ring[kitem % stages] != kitem:
-            raise Violation(f"S tail of tile {t} reads ring item {ring[kitem % stages]}, not {kitem}")
-        if q_buf[t] != u:
-            raise Violation(f"S tail of tile {t} unit {u} reads Q of unit {q_buf[t]}")
-        tail = s_tail_buf[t]
-        if tail is not None and tail[0] == "P" and p_tail_used[t] != tail[1:]:
-            raise Violation(f"S tail of tile {t} overwrites P of {tail[1:]} before its P.V read it")
-        if tail is not None and tail[0] != "P" and s_read[t] != tail:
-            raise Violation(f"S tail of tile {t} overwritten before the softmax read {tail}")
-        s_tail_buf[t] = (u, j)
-
-    def run_pv_tail(u, t, j, vitem):
-        if ring[vitem % stages] != vitem:
-            raise Violation(f"P.V of tile {t} reads ring item {ring[vitem % stages]}, not {vitem}")
-        if s_tail_buf[t] != ("P", u, j):
-            raise Violation(f"P.V of tile {t} block {(u, j)} reads P's last keys of {s_tail_buf[t]}")
-        p_tail_used[t] = (u, j)
-        tail_done[t].add((u, j))
-
-    def run_pv_main(u, t, j, vitem):
-        if ring[vitem % stages] != vitem:
-            raise Violation(f"P.V of tile {t} reads ring item {ring[vitem % stages]}, not {vitem}")
-        if p_main[t] != (u, j):
-            raise Violation(f"P.V of tile {t} block {(u, j)} reads P of {p_main[t]}")
-        p_main_used[t] = (u, j)
-        pv_done[t].add((u, j))
+    def run_pv(t, u, j, vitem, part):
+        check_ring(vitem, f"P.V of tile {t} {(u, j)}")
+        if coupled:
+            held = s_reg[t]["main"]
+        elif split and part == "tail":
+            held = s_reg[t]["tail"]
+        else:
+            held = ("P", *p_buf[t]) if p_buf[t] is not None else None
+        if held != ("P", u, j):
+            raise Violation(f"P.V ({part}) of tile {t} block {(u, j)} reads {held}")
+        ran[t].add((part, u, j))
 
     def run_release(slot):
         ring[slot] = None
@@ -406,21 +204,27 @@ def simulate_split(units, stages, mutate=None, seed=0):
     def commit(name):
         issue(lambda: bar(name).arrive())
 
+    # ------------------------------------------------------------ MMA warp
     def mma():
         item, uit, npv = 0, 0, 0
         ns = [0, 0]
+        pr = [0, 0]
 
-        def s_main(u, t, j, kitem):
+        def s_after_free(t, u, j, kitem):
             if ns[t] > 0 and mutate != "mma_skips_s_free":
-                yield ("s_free", t), (ns[t] - 1) & 1
+                parity = (ns[t] - 1) & 1
+                if mutate == "mma_s_free_wrong_parity":
+                    parity ^= 1
+                yield ("s_free", t), parity
             ns[t] += 1
-            issue(run_s_main, u, t, j, kitem)
+            issue(run_s, t, u, j, kitem, "main")
 
-        def s_tail(u, t, j, kitem):
-            issue(run_s_tail, u, t, j, kitem)
-            commit(("s_full", t))
+        def s0_coupled(u, j, kitem, J0):
+            if j < J0:
+                issue(run_s, 0, u, j, kitem, "main")
+                commit(("s_full", 0))
 
-        for u, (J, _) in enumerate(units):
+        for u, (J, skip0) in enumerate(units):
             if J == 0:
                 continue
             yield ("q_full", 0), uit & 1
@@ -428,94 +232,145 @@ def simulate_split(units, stages, mutate=None, seed=0):
             base = item
             item += 2 * J
             yield ("kv_full", base % stages), (base // stages) & 1
-            for t in range(2):
-                yield from s_main(u, t, 0, base)
-                s_tail(u, t, 0, base)
-            issue(run_release, base % stages)
-            if J == 1:
-                commit(("q_empty", 0)), commit(("q_empty", 1))
-            for j in range(J):
-                iv, ik = base + 2 * j + 1, base + 2 * j + 2
-                nxt = j + 1 < J
-                if nxt:
-                    yield ("kv_full", ik % stages), (ik // stages) & 1
-                    yield from s_main(u, 0, j + 1, ik)
-                    yield from s_main(u, 1, j + 1, ik)
-                yield ("kv_full", iv % stages), (iv // stages) & 1
+            if coupled:
+                J0 = J - 1 if skip0 else J
                 for t in range(2):
-                    yield ("p_tail", t), npv & 1
-                    if mutate == "mma_tail_before_pv" and nxt:
-                        s_tail(u, t, j + 1, ik)
-                    issue(run_pv_tail, u, t, j, iv)
-                    commit(("pt_done", t))
-                    if nxt and mutate != "mma_tail_before_pv":
-                        s_tail(u, t, j + 1, ik)
-                for t in range(2):
-                    yield ("p_ready", t), npv & 1
-                    issue(run_pv_main, u, t, j, iv)
-                    commit(("p_free", t))
+                    issue(run_s, t, u, 0, base, "main")
+                    commit(("s_full", t))
+                issue(run_release, base % stages)
+                if J == 1:
+                    commit(("q_empty", 0)), commit(("q_empty", 1))
+                for j in range(J):
+                    iv, ik = base + 2 * j + 1, base + 2 * j + 2
+                    yield ("kv_full", iv % stages), (iv // stages) & 1
+                    if j + 1 < J and mutate == "mma_s_before_pv":
+                        yield ("kv_full", ik % stages), (ik // stages) & 1
+                        s0_coupled(u, j + 1, ik, J0)
+                    if j < J0:
+                        yield ("p_ready", 0), pr[0] & 1
+                        pr[0] += 1
+                        issue(run_pv, 0, u, j, iv, "main")
+                        if j == J0 - 1:
+                            commit(("o_final", 0))
+                    if j + 1 < J and mutate != "mma_s_before_pv":
+                        yield ("kv_full", ik % stages), (ik // stages) & 1
+                        s0_coupled(u, j + 1, ik, J0)
+                    yield ("p_ready", 1), pr[1] & 1
+                    pr[1] += 1
+                    issue(run_pv, 1, u, j, iv, "main")
+                    issue(run_release, iv % stages)
                     if j == J - 1:
-                        commit(("o_final", t))
-                issue(run_release, iv % stages)
-                if nxt:
-                    issue(run_release, ik % stages)
-                    if j + 2 == J:
-                        commit(("q_empty", 0)), commit(("q_empty", 1))
-                npv += 1
+                        commit(("o_final", 1))
+                    if j + 1 < J:
+                        issue(run_s, 1, u, j + 1, ik, "main")
+                        commit(("s_full", 1))
+                        issue(run_release, ik % stages)
+                        if j + 2 == J:
+                            commit(("q_empty", 0)), commit(("q_empty", 1))
+            else:
+                for t in range(2):
+                    yield from s_after_free(t, u, 0, base)
+                    if split:
+                        # The previous unit's last P.V steps, already issued,
+                        # read P's last keys before this overwrites them.
+                        issue(run_s, t, u, 0, base, "tail")
+                    commit(("s_full", t))
+                issue(run_release, base % stages)
+                if J == 1:
+                    commit(("q_empty", 0)), commit(("q_empty", 1))
+                for j in range(J):
+                    iv, ik = base + 2 * j + 1, base + 2 * j + 2
+                    nxt = j + 1 < J
+                    if nxt:
+                        yield ("kv_full", ik % stages), (ik // stages) & 1
+                        for t in range(2):
+                            yield from s_after_free(t, u, j + 1, ik)
+                            if not split:
+                                commit(("s_full", t))
+                        if not split:
+                            issue(run_release, ik % stages)
+                            if j + 2 == J:
+                                commit(("q_empty", 0)), commit(("q_empty", 1))
+                    yield ("kv_full", iv % stages), (iv // stages) & 1
+                    if split:
+                        for t in range(2):
+                            yield ("p_tail", t), npv & 1
+                            if mutate == "mma_tail_before_pv" and nxt:
+                                issue(run_s, t, u, j + 1, ik, "tail")
+                                commit(("s_full", t))
+                            issue(run_pv, t, u, j, iv, "tail")
+                            commit(("pt_done", t))
+                            if nxt and mutate != "mma_tail_before_pv":
+                                issue(run_s, t, u, j + 1, ik, "tail")
+                                commit(("s_full", t))
+                    for t in range(2):
+                        yield ("p_ready", t), npv & 1
+                        issue(run_pv, t, u, j, iv, "main")
+                        commit(("p_free", t))
+                        if j == J - 1:
+                            commit(("o_final", t))
+                    issue(run_release, iv % stages)
+                    if split and nxt:
+                        issue(run_release, ik % stages)
+                        if j + 2 == J:
+                            commit(("q_empty", 0)), commit(("q_empty", 1))
+                    npv += 1
             uit += 1
         mma_done[0] = True
 
-    def rescale(t, u, j, done):
-        """O_t is rescaled: every P.V step that accumulates into it so far must
-        have run (`done` lists the steps issued before this point)."""
-        for kind, key in done:
-            if key not in (tail_done[t] if kind == "tail" else pv_done[t]):
-                raise Violation(f"O of tile {t} rescaled at {(u, j)} while P.V {kind} {key} "
-                                f"has not run")
+    # ------------------------------------------------------------ softmax
+    def rescale(t, u, j, steps):
+        for step in steps:
+            if step not in ran[t]:
+                raise Violation(f"O of tile {t} rescaled at {(u, j)} before P.V step {step} ran")
 
     def softmax(t):
         sit, np_, uit = 0, 0, 0
-        prev = None
-        for u, (J, _) in enumerate(units):
+        for u, (J, skip0) in enumerate(units):
             if J == 0:
                 continue
-            for j in range(J):
+            nb = J - 1 if (coupled and skip0 and t == 0) else J
+            earlier = []                 # P.V steps of this unit issued so far
+            for j in range(nb):
                 yield ("s_full", t), sit & 1
                 sit += 1
-                if s_main_buf[t] != (u, j) or s_tail_buf[t] != (u, j):
-                    raise Violation(f"softmax {t} expected S of {(u, j)}, TMEM holds "
-                                    f"{s_main_buf[t]} / {s_tail_buf[t]}")
+                want = ("S", u, j)
+                if s_reg[t]["main"] != want or (split and s_reg[t]["tail"] != want):
+                    raise Violation(f"softmax {t} expected S of {(u, j)}, TMEM holds {s_reg[t]}")
                 s_read[t] = (u, j)
+                if coupled:
+                    if j > 0 and retake_rng.random() < 0.15:
+                        rescale(t, u, j, earlier)
+                    s_reg[t]["main"] = ("P", u, j)       # P over S (already read)
+                    bar(("p_ready", t)).arrive()
+                    earlier.append(("main", u, j))
+                    continue
                 bar(("s_free", t)).arrive()
                 pfree_seen = np_ == 0
-                # A retake found on the last keys: wait for the previous P.V,
-                # then rescale (O holds the unit's earlier blocks only).
-                if j > 0 and redo_rng.random() < 0.15:
+                if j > 0 and retake_rng.random() < 0.15:
                     if not pfree_seen and mutate != "softmax_skips_p_free":
                         yield ("p_free", t), (np_ - 1) & 1
                         pfree_seen = True
-                    rescale(t, u, j, [("main", prev)])
-                s_tail_buf[t] = ("P", u, j)   # P's last keys over S's tail (already read)
-                bar(("p_tail", t)).arrive()
+                    rescale(t, u, j, earlier)
+                if split:
+                    s_reg[t]["tail"] = ("P", u, j)       # P's last keys over S's tail (read)
+                    bar(("p_tail", t)).arrive()
                 if not pfree_seen and mutate != "softmax_skips_p_free":
                     yield ("p_free", t), (np_ - 1) & 1
-                if p_main[t] is not None and p_main_used[t] != p_main[t]:
-                    raise Violation(f"P of tile {t} block {p_main[t]} overwritten before its P.V")
-                p_main[t] = (u, j)
-                # A retake found on the whole block: O already takes P.V over
-                # this block's last keys; wait for it (pt_done), then rescale.
-                if redo_rng.random() < 0.15:
+                if p_buf[t] is not None and ("main", *p_buf[t]) not in ran[t]:
+                    raise Violation(f"P of tile {t} block {p_buf[t]} overwritten before its P.V")
+                p_buf[t] = (u, j)
+                if split and retake_rng.random() < 0.15:
                     if mutate != "softmax_skips_pt_done":
                         yield ("pt_done", t), np_ & 1
-                    steps = [("tail", (u, j))] + ([("main", prev)] if j > 0 else [])
-                    rescale(t, u, j, steps)
+                    rescale(t, u, j, earlier + [("tail", u, j)])
                 bar(("p_ready", t)).arrive()
                 np_ += 1
-                prev = (u, j)
+                earlier += [("tail", u, j), ("main", u, j)] if split else [("main", u, j)]
             yield ("o_final", t), uit & 1
-            missing = [j for j in range(J) if (u, j) not in pv_done[t]]
+            missing = [s for s in earlier if s not in ran[t]]
             if missing:
-                raise Violation(f"tile {t} reads O of unit {u} before P.V of blocks {missing}")
+                raise Violation(f"tile {t} reads O of unit {u} before P.V steps {missing}")
             uit += 1
 
     roles = {"load": load(), "mma": mma(), "tensor": tensor(), "softmax0": softmax(0),
@@ -531,47 +386,47 @@ def random_units(rng, causal):
     return units
 
 
-@pytest.mark.parametrize("decoupled,stages,split", [(False, 4, False), (True, 8, False),
-                                                     (True, 4, False), (True, 8, True),
-                                                     (True, 4, True)])
-def test_protocol_completes_and_is_safe(decoupled, stages, split):
-    rng = random.Random(1000 + stages + 10 * decoupled + 100 * split)
+@pytest.mark.parametrize("order,stages", [("coupled", 4), ("decoupled", 8), ("decoupled", 4),
+                                          ("split", 8), ("split", 4)])
+def test_protocol_completes_and_is_safe(order, stages):
+    rng = random.Random(1000 + stages + 10 * ORDERS.index(order))
     for case in range(150):
-        units = random_units(rng, causal=not decoupled)
-        stuck = simulate(units, decoupled, stages, seed=case, split=split)
+        units = random_units(rng, causal=order == "coupled")
+        stuck = simulate(units, order, stages, seed=case)
         assert not stuck, (units, stuck)
 
 
-@pytest.mark.parametrize("mutation,decoupled,split", [
-    ("mma_skips_s_free", True, False),
-    ("mma_s_free_wrong_parity", True, False),
-    ("softmax_skips_p_free", True, False),
-    ("load_skips_empty_wait", True, False),
-    ("load_skips_empty_wait", False, False),
-    ("load_skips_q_empty", False, False),
-    ("load_skips_q_empty", True, False),
-    ("mma_skips_s_free", True, True),
-    ("softmax_skips_p_free", True, True),
-    ("mma_tail_before_pv", True, True),
-    ("softmax_skips_pt_done", True, True),
+@pytest.mark.parametrize("mutation,order", [
+    ("load_skips_empty_wait", "coupled"),
+    ("load_skips_q_empty", "coupled"),
+    ("mma_s_before_pv", "coupled"),
+    ("mma_skips_s_free", "decoupled"),
+    ("mma_s_free_wrong_parity", "decoupled"),
+    ("softmax_skips_p_free", "decoupled"),
+    ("load_skips_empty_wait", "decoupled"),
+    ("load_skips_q_empty", "decoupled"),
+    ("mma_skips_s_free", "split"),
+    ("mma_s_free_wrong_parity", "split"),
+    ("softmax_skips_p_free", "split"),
+    ("mma_tail_before_pv", "split"),
+    ("softmax_skips_pt_done", "split"),
+    ("load_skips_empty_wait", "split"),
+    ("load_skips_q_empty", "split"),
 ])
-def test_protocol_mutations_are_caught(mutation, decoupled, split):
+def test_protocol_mutations_are_caught(mutation, order):
     """Each mutation must end in a safety violation or a role that never
     finishes, for some unit sequence."""
     rng = random.Random(7)
-    caught = False
-    for case in range(200):
-        units = random_units(rng, causal=not decoupled)
+    stages = 4 if order == "coupled" else 8
+    for case in range(300):
+        units = random_units(rng, causal=order == "coupled")
         try:
-            stuck = simulate(units, decoupled, 4 if not decoupled else 8, mutate=mutation, seed=case,
-                             split=split)
+            stuck = simulate(units, order, stages, mutate=mutation, seed=case)
         except Violation:
-            caught = True
-            break
+            return
         if stuck:
-            caught = True
-            break
-    assert caught, mutation
+            return
+    pytest.fail(f"{mutation} ({order}) was not caught")
 
 
 def test_two_p_buffers_on_one_barrier_deadlock():
