@@ -1,6 +1,7 @@
 """CPU checks of the constructed retake rows (no GPU): each head's scores take
 the path of the kernel's reference rule its parity test relies on."""
 import numpy as np
+import pytest
 
 from retake_cases import LOG2E, SUM_LIMIT, reference_path, retake_scores
 
@@ -43,9 +44,10 @@ def _bf16(x):
     return torch.from_numpy(np.asarray(x, dtype=np.float32)).to(torch.bfloat16).double().numpy()
 
 
-def early_tail_row(s, v):
+def early_tail_row(s, v, tail_first=True):
     """One row: s natural-unit scores (scale folded in), v [N, d] values.
-    Returns (O, lse)."""
+    Returns (O, lse).  tail_first=False is the d = 128 kernel's order: the
+    whole block is weighed and tested at once (its "last keys" are none)."""
     x_all = np.asarray(s, dtype=np.float64) * LOG2E
     m, ell, ellt = -np.inf, 0.0, 0.0
     o = np.zeros(v.shape[1])
@@ -53,24 +55,25 @@ def early_tail_row(s, v):
         x, vb = x_all[128 * j:128 * j + 128], v[128 * j:128 * j + 128]
         if m == -np.inf:
             m = x.max()
-        p_tail = np.exp2(x[96:] - m)
+        t0 = 96 if tail_first else 128
+        p_tail = np.exp2(x[t0:] - m)
         if p_tail.sum() > SUM_LIMIT:
             alpha = np.exp2(m - max(m, x.max()))
             m = max(m, x.max())
             o, ellt, ell = o * alpha, ellt * alpha, ell * alpha
-            p_tail = np.exp2(x[96:] - m)
+            p_tail = np.exp2(x[t0:] - m)
         pb = _bf16(p_tail)
-        o, ellt = o + pb @ vb[96:], ellt + pb.sum()
+        o, ellt = o + pb @ vb[t0:], ellt + pb.sum()
         sum_tail = p_tail.sum()
-        p_main = np.exp2(x[:96] - m)
+        p_main = np.exp2(x[:t0] - m)
         if sum_tail + p_main.sum() > SUM_LIMIT:
             alpha = np.exp2(m - max(m, x.max()))
             m = max(m, x.max())
             o, ellt, ell = o * alpha, ellt * alpha, ell * alpha
             sum_tail *= alpha
-            p_main = np.exp2(x[:96] - m)
+            p_main = np.exp2(x[:t0] - m)
         pb = _bf16(p_main)
-        o, ellt = o + pb @ vb[:96], ellt + pb.sum()
+        o, ellt = o + pb @ vb[:t0], ellt + pb.sum()
         ell += sum_tail + p_main.sum()
     return o / ellt, (m + np.log2(ell)) / LOG2E
 
@@ -85,23 +88,25 @@ def _oracle_row(s, v):
     return O[0, 0, 0], L[0, 0, 0]
 
 
-def test_early_tail_algorithm_matches_the_oracle_on_the_retake_rows():
+@pytest.mark.parametrize("tail_first", [True, False])
+def test_early_tail_algorithm_matches_the_oracle_on_the_retake_rows(tail_first):
     rng = np.random.default_rng(5)
     v = _bf16(rng.standard_normal((512, 64)))
     for head in (0, 1, 2):
         s = retake_scores(head).double().numpy()
-        o, lse = early_tail_row(s, v)
+        o, lse = early_tail_row(s, v, tail_first)
         O_ref, L_ref = _oracle_row(s, v)
         assert np.abs(o - O_ref).max() < 1e-2      # bf16 P: ~2^-9 relative per weight
         assert abs(lse - L_ref) < 1e-6             # l is summed in full precision here
 
 
-def test_early_tail_algorithm_matches_the_oracle_on_random_rows():
+@pytest.mark.parametrize("tail_first", [True, False])
+def test_early_tail_algorithm_matches_the_oracle_on_random_rows(tail_first):
     rng = np.random.default_rng(6)
     for spread in (1.0, 8.0, 40.0):
         s = _bf16(rng.standard_normal(1024) * spread)
         v = _bf16(rng.standard_normal((1024, 64)))
-        o, lse = early_tail_row(s, v)
+        o, lse = early_tail_row(s, v, tail_first)
         O_ref, L_ref = _oracle_row(s, v)
         assert np.abs(o - O_ref).max() < 1e-2
         assert abs(lse - L_ref) < 1e-6
